@@ -1,0 +1,547 @@
+#!/usr/bin/env python3
+"""Benchmark of the THD zigzag <-> contiguous layout conversion on one GB300.
+
+A step is one pass of the hot path over one packed microbatch: zigzag
+partition indices, the route in both directions (validation, interval
+counts, identity flags), then every simulated layer's swap pair
+(zigzag->contiguous, contiguous->zigzag) on the hidden states.  The default
+workload is the log-normal 128K-token packing with cp=4 and 4 KiB rows
+(x bf16 [131072, 16, 128]) reused by 48 layers; the working set (1 GiB in
++ 1 GiB out ping-pong) is far larger than L2, so no flush is needed.
+
+value      = swap payload bytes (2 * T * row_bytes per swap, read + write)
+             per second of whole-step device time, max over ranks.
+e2e        = the same with the step's input copied host->device from pinned
+             memory and the result copied back inside the timed region.
+roofline   = the swap kernel alone: payload bytes per launch / its average
+             launch time, against the measured copy bandwidth.
+cpu_baseline / --impl reference = the CPU oracle on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl thd|reference]
+    torchrun --nproc-per-node N bench.py --gpus N ...   (one rank per GPU,
+    independent microbatches: weak scaling, no collective on the data path)
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+import torch.distributed as dist  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "THD zigzag<->contiguous swap HBM GB/s & % of peak; route-build µs per microbatch"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["thd", "reference"], default="thd")
+    p.add_argument("--workload", default="lognorm128k", choices=[w.name for w in W.WORKLOADS])
+    p.add_argument("--layers", type=int, default=None, help="swap pairs per step (default: 48; pipeline 1)")
+    p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def setup_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world, device=None):
+    if world > 1:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """Largest value over all ranks (elapsed times: the slowest rank decides)."""
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def swap_traffic_record():
+    """dram bytes per swap launch from the committed ncu summary, or None when
+    the summary is missing or the copy kernel's source changed since."""
+    path = os.path.join(ROOT, "profiles", "copy_rows_swap_lognorm128k.md")
+    src = os.path.join(ROOT, "context_packed_sequence_gb300", "csrc", "copy.cu")
+    try:
+        text = open(path).read()
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("copy.cu sha256") != digest:
+        return None
+    try:
+        return int(fields["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# inputs
+# ---------------------------------------------------------------------------
+
+def make_inputs(w, device, rank):
+    """(cu list, T, raw tokens or None) of the workload; x is drawn separately."""
+    if w.name == "pipeline":
+        raw = W.raw_pipeline_tokens(w.seed + 1000 * rank)
+        return None, None, raw
+    cu = W.boundaries(W.doc_lengths(w.name))
+    return cu, cu[-1], None
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_thd(args, rank, world, local):
+    import context_packed_sequence_gb300 as thd
+    from context_packed_sequence_gb300 import _lib as L
+    import ctypes
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = W.BY_NAME[args.workload]
+    layers = args.layers if args.layers is not None else (1 if w.name == "pipeline" else 48)
+    cp = w.cp
+    stream = torch.cuda.current_stream(device)
+    sp = stream.cuda_stream
+    lib = L.load()
+
+    cu_list, T, raw = make_inputs(w, device, rank)
+    status = thd.new_status(device)
+    extra = None
+    if raw is not None:
+        raw_d = torch.from_numpy(raw).to(device)
+        B, S = raw.shape
+        tok, cu_v, cu_d = thd.pack_docs(raw_d, W.EOD_ID, 2 * cp, pad_id=0)   # data prep, untimed
+        T = int(tok.numel())
+        n_docs = cu_d.numel() - 1
+        cap_tok, cap_docs = B * S * 2 * cp, B * S + 1
+        ptok = torch.empty(cap_tok, dtype=torch.int32, device=device)
+        pcu_v = torch.empty(cap_docs, dtype=torch.int32, device=device)
+        pcu = torch.empty(cap_docs, dtype=torch.int32, device=device)
+        counts = torch.zeros(2, dtype=torch.int64, device=device)
+        ws = torch.empty(lib.thd_pack_docs_workspace_bytes(B), dtype=torch.uint8, device=device)
+        labels = torch.empty((w.mtp_depth + 1, T), dtype=torch.int32, device=device)
+        lmask = torch.empty((w.mtp_depth + 1, T), dtype=torch.uint8, device=device)
+        valid = torch.empty((T,), dtype=torch.uint8, device=device)
+        extra = dict(raw=raw_d, B=B, S=S, ptok=ptok, pcu_v=pcu_v, pcu=pcu, counts=counts, ws=ws,
+                     labels=labels, lmask=lmask, valid=valid, cap_tok=cap_tok, cap_docs=cap_docs)
+    else:
+        cu_d = torch.tensor(cu_list, dtype=torch.int32, device=device)
+        n_docs = len(cu_list) - 1
+    row_bytes = w.row_bytes
+    x = W.payload_device(w.seed + 1000 * rank, T, w.hidden, device)
+    y = torch.empty_like(x)
+    fwd = thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device)
+    bwd = thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device)
+    pidx = torch.empty((cp, T // cp), dtype=torch.int32, device=device)
+    swap_bytes = 2 * T * row_bytes
+    launches_per_step = 3 + 2 * layers + (3 if extra is not None else 0)
+
+    def front(s):
+        """Everything before the swaps: (packing and labels,) partition, routes."""
+        if extra is not None:
+            e = extra
+            lib.thd_pack_docs(e["raw"].data_ptr(), e["B"], e["S"], W.EOD_ID, 0, 0, 2 * cp, 0, e["ptok"].data_ptr(),
+                              e["cap_tok"], e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), e["cap_docs"],
+                              e["counts"].data_ptr(), e["ws"].data_ptr(), e["ws"].numel(), status.data_ptr(), s)
+            lib.thd_roll_labels(e["ptok"].data_ptr(), e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), n_docs, T,
+                                w.mtp_depth, 0, e["labels"].data_ptr(), e["lmask"].data_ptr(),
+                                e["valid"].data_ptr(), status.data_ptr(), s)
+        lib.thd_partition_indices(cu_d.data_ptr(), n_docs, T, cp, -1, pidx.data_ptr(), status.data_ptr(), s)
+        lib.thd_route_build(cu_d.data_ptr(), n_docs, T, cp, 0, ctypes.byref(fwd.c), status.data_ptr(), s)
+        lib.thd_route_build(cu_d.data_ptr(), n_docs, T, cp, 1, ctypes.byref(bwd.c), status.data_ptr(), s)
+
+    def swaps(s, a, b):
+        for _ in range(layers):
+            lib.thd_swap(a.data_ptr(), b.data_ptr(), row_bytes, ctypes.byref(fwd.c), status.data_ptr(), s)
+            lib.thd_swap(b.data_ptr(), a.data_ptr(), row_bytes, ctypes.byref(bwd.c), status.data_ptr(), s)
+
+    # warm-up
+    for _ in range(args.warmup):
+        front(sp)
+        swaps(sp, x, y)
+    torch.cuda.synchronize(device)
+    code = thd.status_read(status)
+    if code != 0:
+        raise RuntimeError(f"device status {code} after warm-up")
+
+    # timed region
+    n_ev = args.steps
+    ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev + 1)]
+    ev_sw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    clocks = ClockSampler(device.index).start() if rank == 0 else None
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    ev_step[0].record(stream)
+    for i in range(n_ev):
+        front(sp)
+        ev_sw[i][0].record(stream)
+        swaps(sp, x, y)
+        ev_sw[i][1].record(stream)
+        ev_step[i + 1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    clock_rec = clocks.stop() if clocks is not None else None
+    step_ms_local = ev_step[0].elapsed_time(ev_step[-1])
+    swap_ms_total = sum(a.elapsed_time(b) for a, b in ev_sw)
+    code = thd.status_read(status)
+    if code != 0:
+        raise RuntimeError(f"device status {code} in the timed region")
+
+    total_ms = max_over_ranks(step_ms_local, world, device)
+    bytes_all = sum_over_ranks(float(swap_bytes * 2 * layers * n_ev), world, device)
+    value = bytes_all / (total_ms / 1e3) / 1e9
+    swap_us = swap_ms_total * 1e3 / (2 * layers * n_ev)
+    achieved = swap_bytes / (swap_us * 1e-6) / 1e9
+
+    # route build alone: CUDA events around each build, the GPU kept busy so
+    # host launch latency is not counted; median of 50
+    rb = {"zigzag_to_contiguous": [], "contiguous_to_zigzag": [], "partition": []}
+    for it in range(60):
+        torch.cuda._sleep(200_000)
+        e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        e0.record(stream)
+        lib.thd_route_build(cu_d.data_ptr(), n_docs, T, cp, 0, ctypes.byref(fwd.c), status.data_ptr(), sp)
+        e1.record(stream)
+        lib.thd_route_build(cu_d.data_ptr(), n_docs, T, cp, 1, ctypes.byref(bwd.c), status.data_ptr(), sp)
+        e2.record(stream)
+        lib.thd_partition_indices(cu_d.data_ptr(), n_docs, T, cp, -1, pidx.data_ptr(), status.data_ptr(), sp)
+        e3.record(stream)
+        torch.cuda.synchronize(device)
+        if it >= 10:
+            rb["zigzag_to_contiguous"].append(e0.elapsed_time(e1) * 1e3)
+            rb["contiguous_to_zigzag"].append(e1.elapsed_time(e2) * 1e3)
+            rb["partition"].append(e2.elapsed_time(e3) * 1e3)
+    route_us = {k: round(statistics.median(v), 2) for k, v in rb.items()}
+    route_us["both_directions"] = round(route_us["zigzag_to_contiguous"] + route_us["contiguous_to_zigzag"], 2)
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes)
+
+    peak, peak_kind = measured_peak()
+    traffic = swap_traffic_record()
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": n_ev,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / n_ev, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "payload": "bf16 rows moved as raw 16-byte units",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name,
+            "description": w.description,
+            "cp_size": cp,
+            "T": T,
+            "num_docs": n_docs,
+            "row_bytes": row_bytes,
+            "layers": layers,
+            "swaps_per_step": 2 * layers,
+            "parallelism": f"{world} independent microbatch(es), one per GPU; {cp} virtual CP ranks per GPU",
+            "l2": f"no flush: working set {2 * T * row_bytes / 2**30:.2f} GiB > L2 {L2_BYTES / 2**20:.0f} MiB",
+        },
+        "rows_per_s": round(T * 2 * layers * n_ev * world / (total_ms / 1e3), 1),
+        "route_build_us": route_us,
+        "swap_us_per_launch": round(swap_us, 2),
+        "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "copy_rows_kernel<uint4, SwapMap> (thd_swap)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_kind": f"{peak_kind} copy bandwidth (read+write)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": swap_bytes,
+        },
+        "gpu_launches": launches_per_step * n_ev,
+        "clocks": clock_rec,
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    return result, dict(x=x, T=T, cu=cu_d, w=w, row_bytes=row_bytes)
+
+
+def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes, steps=5, warm=2):
+    """Per step: pinned host -> device copy of x and cu, route build, the swap
+    pairs, device -> host copy of the result; timed with events around all."""
+    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_host.copy_(x)
+    cu_host = cu_d.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    xd = torch.empty_like(x)
+    yd = torch.empty_like(x)
+    cud = torch.empty_like(cu_d)
+    st = thd.new_status(device)
+    fwd = thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device)
+    bwd = thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        xd.copy_(x_host, non_blocking=True)
+        cud.copy_(cu_host, non_blocking=True)
+        thd.route_build(cud, T, cp, thd.ZIGZAG_TO_CONTIGUOUS, status=st, route=fwd)
+        thd.route_build(cud, T, cp, thd.CONTIGUOUS_TO_ZIGZAG, status=st, route=bwd)
+        for _ in range(layers):
+            thd.swap(xd, fwd, out=yd, status=st)
+            thd.swap(yd, bwd, out=xd, status=st)
+        out_host.copy_(xd, non_blocking=True)
+
+    for _ in range(warm):
+        step()
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    if thd.status_read(st) != 0 or not torch.equal(out_host, x.cpu()):
+        raise RuntimeError("e2e pass produced a wrong result")
+    bytes_all = sum_over_ranks(float(swap_bytes * 2 * layers * steps), world, device)
+    return {"value": round(bytes_all / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": int(x.numel() * x.element_size() + cu_d.numel() * 4),
+            "d2h_bytes_per_step": int(x.numel() * x.element_size()),
+            "ms_per_step": round(ms / steps, 3), "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_payload(w, T):
+    """The workload's payload as host bytes [T, row_bytes] (drawn on the host)."""
+    x = W.payload_host(w.seed, T, w.hidden)
+    return x.contiguous().view(torch.uint8).reshape(T, -1).numpy()
+
+
+def oracle_cu(w):
+    if w.name == "pipeline":
+        import oracle
+        raw = W.raw_pipeline_tokens(w.seed)
+        _, _, cu = oracle.pack_docs(raw.tolist(), W.EOD_ID, 2 * w.cp, pad_id=0)
+        return cu
+    return W.boundaries(W.doc_lengths(w.name))
+
+
+def oracle_step(cu, T, cp, direction, xb):
+    """One bounded sample: the oracle builds one direction's route token by
+    token and applies it (pack -> all-to-all -> scatter) to the full payload."""
+    import oracle
+    rt = oracle.build_route(cu, T, cp, direction)
+    _, _, out = oracle.apply_route(xb, rt)
+    return out
+
+
+def run_cpu_baseline(w, budget_s):
+    cu = oracle_cu(w)
+    T = cu[-1]
+    xb = oracle_payload(w, T)
+    swap_bytes = 2 * T * w.row_bytes
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(cu, T, w.cp, done % 2, xb)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(done * swap_bytes / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} oracle swap(s) of the full {w.name} workload (T={T}, {w.row_bytes} B rows), "
+                      f"each = per-token route build of one direction + pack/all-to-all/scatter row by row, "
+                      f"pure Python on 1 thread, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = W.BY_NAME[args.workload]
+    cu = oracle_cu(w)
+    T = cu[-1]
+    xb = oracle_payload(w, T)
+    swap_bytes = 2 * T * w.row_bytes
+    for i in range(args.warmup):
+        oracle_step(cu, T, w.cp, i % 2, xb)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(cu, T, w.cp, i % 2, xb)
+    el = time.perf_counter() - t0
+    value = args.steps * swap_bytes / el / 1e9
+    sample = (f"each step = one oracle swap of the full {w.name} workload (T={T}, {w.row_bytes} B rows): "
+              f"per-token route build of one direction + pack/all-to-all/scatter row by row, 1 thread")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3 / max(args.steps, 1), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "cp_size": w.cp, "T": T,
+                   "row_bytes": w.row_bytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local = setup_dist(args)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, rank, world)
+            if res is not None:
+                print(json.dumps(res), flush=True)
+            return
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py: the thd arm needs a CUDA GPU")
+        res, _ = run_thd(args, rank, world, local)
+        if rank == 0:
+            if not args.no_cpu_baseline and world == 1:
+                res["cpu_baseline"] = run_cpu_baseline(W.BY_NAME[args.workload], args.cpu_budget)
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1 and dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,17 @@
+"""Packed-sequence (THD) context-parallel layout conversion for one GB300.
+
+All cp virtual context-parallel ranks live in one device buffer, so the
+zigzag <-> contiguous all-to-all is an on-device row permutation.  The CUDA
+library ``libthd.so`` (C ABI in ``include/thd.h``) does all the work; this
+package is its thin torch binding.
+"""
+
+from .api import (  # noqa: F401
+    ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG, ThdError, Route, RouteCache,
+    new_status, status_clear, status_read, check_status,
+    route_build, partition_indices, swap, pack, a2a_local, scatter,
+    roll_labels, pack_docs, zigzag_contiguous_thd_swap,
+)
+from . import _lib  # noqa: F401
+
+__version__ = "0.1.0"

@@ -1,0 +1,335 @@
+"""Torch-facing binding of libthd.
+
+PyTorch supplies device memory and the current stream; every step of the
+layout conversion runs in libthd's CUDA kernels.  Functions here only check
+shapes, allocate outputs and pass pointers through the C ABI.
+
+Names follow the pages: "[Task32] feat: fla mcore chunkwise cp stage 3"
+(Relax PR #273) for the route, its cache and the layout swap,
+"Packed Sequence 与上下文并行" for partitioning, packing and labels.
+"""
+
+from __future__ import annotations
+
+import contextlib
+import ctypes
+import os
+
+import torch
+
+from . import _lib as L
+
+ZIGZAG_TO_CONTIGUOUS = L.ZIGZAG_TO_CONTIGUOUS
+CONTIGUOUS_TO_ZIGZAG = L.CONTIGUOUS_TO_ZIGZAG
+
+_NVTX = os.environ.get("THD_NVTX", "0") == "1"
+
+
+class ThdError(ValueError):
+    """A failed check; ``kind`` is the status name (e.g. 'len_not_divisible')."""
+
+    def __init__(self, code: int, what: str = ""):
+        self.code = int(code)
+        self.kind = L.STATUS_NAMES.get(self.code, f"status_{self.code}")
+        msg = L.load().thd_status_string(self.code).decode()
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+@contextlib.contextmanager
+def _range(name):
+    """NVTX range around a layout step when THD_NVTX=1 (the pages wrap the
+    conversion in an NVTX range, Relax PR #273 section 2.2)."""
+    if _NVTX:
+        torch.cuda.nvtx.range_push(name)
+        try:
+            yield
+        finally:
+            torch.cuda.nvtx.range_pop()
+    else:
+        yield
+
+
+def _stream(stream=None) -> int:
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _raise_host(code, what):
+    if code == L.ERR_CUDA:
+        err = L.load().thd_last_cuda_error()
+        raise RuntimeError(f"{what}: CUDA error {err}")
+    if code != L.OK:
+        raise ThdError(code, what)
+
+
+def _need_cuda(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+# status word
+# ---------------------------------------------------------------------------
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word (int32[1])."""
+    return torch.zeros(1, dtype=torch.int32, device=device if device is not None else "cuda")
+
+
+def status_clear(status, stream=None):
+    _raise_host(L.load().thd_status_clear(_ptr(status), _stream(stream)), "thd_status_clear")
+
+
+def status_read(status, stream=None) -> int:
+    """Copy the status word to the host; synchronises the stream."""
+    code = ctypes.c_int32(0)
+    _raise_host(L.load().thd_status_read(_ptr(status), ctypes.byref(code), _stream(stream)),
+                "thd_status_read")
+    return code.value
+
+
+def check_status(status, what="thd", stream=None):
+    """Raise ThdError if the device recorded an error (synchronises)."""
+    code = status_read(status, stream)
+    if code != L.OK:
+        raise ThdError(code, what)
+
+
+# ---------------------------------------------------------------------------
+# route
+# ---------------------------------------------------------------------------
+
+class Route:
+    """One direction's all-to-all route for every virtual rank, in one device
+    buffer (fields as in thd_route_t; tensors are views into the buffer)."""
+
+    def __init__(self, T: int, cp: int, direction: int, device=None):
+        lib = L.load()
+        if direction not in (ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG):
+            raise ThdError(L.ERR_BAD_DIRECTION, "Route")
+        nbytes = lib.thd_route_bytes(int(T), int(cp))
+        if nbytes == 0:
+            raise ThdError(L.ERR_INVALID_ARG, f"Route(T={T}, cp={cp})")
+        self.T, self.cp, self.direction = int(T), int(cp), int(direction)
+        self.S = self.T // self.cp
+        self._buf = torch.empty(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
+        self.c = L.ThdRoute()
+        _raise_host(lib.thd_route_bind(ctypes.byref(self.c), self._buf.data_ptr(), nbytes, self.T, self.cp,
+                                       self.direction), "thd_route_bind")
+        base = self._buf.data_ptr()
+
+        def view(addr, n, dtype, shape):
+            off = addr - base
+            nb = n * torch.empty((), dtype=dtype).element_size()
+            return self._buf[off:off + nb].view(dtype).view(shape)
+
+        cp, S = self.cp, self.S
+        self.send_rows = view(self.c.send_rows, cp * S, torch.int32, (cp, S))
+        self.recv_rows = view(self.c.recv_rows, cp * S, torch.int32, (cp, S))
+        self.src_of_dst = view(self.c.src_of_dst, self.T, torch.int32, (self.T,))
+        self.input_split_sizes = view(self.c.input_split_sizes, cp * cp, torch.int32, (cp, cp))
+        self.output_split_sizes = view(self.c.output_split_sizes, cp * cp, torch.int32, (cp, cp))
+        self.send_offsets = view(self.c.send_offsets, cp * (cp + 1), torch.int32, (cp, cp + 1))
+        self.recv_offsets = view(self.c.recv_offsets, cp * (cp + 1), torch.int32, (cp, cp + 1))
+        self.send_identity = view(self.c.send_identity, cp, torch.uint8, (cp,))
+        self.recv_identity = view(self.c.recv_identity, cp, torch.uint8, (cp,))
+
+    @property
+    def device(self):
+        return self._buf.device
+
+
+def route_build(cu_seqlens_padded: torch.Tensor, T: int, cp: int, direction: int, status=None,
+                route: Route | None = None, stream=None) -> Route:
+    """Build one direction's route on the device (no host synchronisation).
+
+    Data-dependent errors land in ``status`` (allocated when None; read it
+    with check_status)."""
+    _need_cuda(cu_seqlens_padded, "cu_seqlens_padded", torch.int32)
+    if route is None:
+        route = Route(T, cp, direction, cu_seqlens_padded.device)
+    if status is None:
+        status = new_status(cu_seqlens_padded.device)
+    route.status = status
+    with _range("thd_route_build"):
+        code = L.load().thd_route_build(_ptr(cu_seqlens_padded), cu_seqlens_padded.numel() - 1, int(T), int(cp),
+                                        int(direction), ctypes.byref(route.c), _ptr(status), _stream(stream))
+    _raise_host(code, "thd_route_build")
+    return route
+
+
+def partition_indices(cu_seqlens_padded: torch.Tensor, T: int, cp: int, rank: int = -1, status=None,
+                      out=None, stream=None) -> torch.Tensor:
+    """Zigzag slice index of one rank ([T/cp]) or of all ranks ([cp, T/cp])."""
+    _need_cuda(cu_seqlens_padded, "cu_seqlens_padded", torch.int32)
+    S = T // cp if cp >= 1 else 0
+    shape = (cp, S) if rank == -1 else (S,)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.int32, device=cu_seqlens_padded.device)
+    if status is None:
+        status = new_status(cu_seqlens_padded.device)
+    code = L.load().thd_partition_indices(_ptr(cu_seqlens_padded), cu_seqlens_padded.numel() - 1, int(T),
+                                          int(cp), int(rank), _ptr(out), _ptr(status), _stream(stream))
+    _raise_host(code, "thd_partition_indices")
+    return out
+
+
+def _copy(fn_name, x, route, out, status, stream):
+    _need_cuda(x, "x")
+    if x.dim() < 1 or x.shape[0] != route.T:
+        raise ValueError(f"x must have {route.T} rows, got shape {tuple(x.shape)}")
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda(out, "out")
+    if out.shape != x.shape or out.dtype != x.dtype:
+        raise ValueError("out must match x in shape and dtype")
+    row_bytes = (x[0].numel() if x.shape[0] else 1) * x.element_size()
+    if x.numel() == 0:
+        return out
+    with _range(fn_name):
+        code = getattr(L.load(), fn_name)(_ptr(x), _ptr(out), row_bytes, ctypes.byref(route.c), _ptr(status),
+                                          _stream(stream))
+    _raise_host(code, fn_name)
+    return out
+
+
+def swap(x, route: Route, out=None, status=None, stream=None):
+    """Fused layout swap: out[q] = x[route.src_of_dst[q]] (rows = x's first dim)."""
+    return _copy("thd_swap", x, route, out, status, stream)
+
+
+def pack(x, route: Route, out=None, status=None, stream=None):
+    """Per-rank send buffers: send[s][j] = x[s][send_rows[s][j]]."""
+    return _copy("thd_pack", x, route, out, status, stream)
+
+
+def a2a_local(send, route: Route, out=None, status=None, stream=None):
+    """The all-to-all between virtual ranks, as block copies in one buffer."""
+    return _copy("thd_a2a_local", send, route, out, status, stream)
+
+
+def scatter(recv, route: Route, out=None, status=None, stream=None):
+    """out[d][recv_rows[d][j]] = recv[d][j]."""
+    return _copy("thd_scatter", recv, route, out, status, stream)
+
+
+# ---------------------------------------------------------------------------
+# labels and packing
+# ---------------------------------------------------------------------------
+
+def roll_labels(tokens, cu_seqlens, cu_seqlens_padded, mtp_depth: int = 0, fill: int = 0, status=None,
+                stream=None):
+    """(labels [D+1, T] int32, loss_mask [D+1, T] uint8, valid_mask [T] uint8)."""
+    for t, n in ((tokens, "tokens"), (cu_seqlens, "cu_seqlens"), (cu_seqlens_padded, "cu_seqlens_padded")):
+        _need_cuda(t, n, torch.int32)
+    if cu_seqlens.numel() != cu_seqlens_padded.numel() or cu_seqlens.numel() < 1:
+        raise ThdError(L.ERR_INVALID_ARG, "roll_labels: boundary arrays differ in length")
+    T = tokens.numel()
+    dev = tokens.device
+    labels = torch.empty((mtp_depth + 1, T), dtype=torch.int32, device=dev)
+    lmask = torch.empty((mtp_depth + 1, T), dtype=torch.uint8, device=dev)
+    valid = torch.empty((T,), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    with _range("thd_roll_labels"):
+        code = L.load().thd_roll_labels(_ptr(tokens), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
+                                        cu_seqlens.numel() - 1, T, int(mtp_depth), int(fill), _ptr(labels),
+                                        _ptr(lmask), _ptr(valid), _ptr(status), _stream(stream))
+    _raise_host(code, "thd_roll_labels")
+    return labels, lmask, valid
+
+
+def pack_docs(raw, eod_id: int, align: int, pad_id: int = 0, raw_pad_id=None, status=None, stream=None,
+              tokens_capacity=None):
+    """Pack raw [B, S] int32 rows into (tokens [T], cu_seqlens, cu_seqlens_padded).
+
+    T and the document count are only known on the device; this call reads
+    them back once (a synchronisation, at data-preparation time)."""
+    _need_cuda(raw, "raw", torch.int32)
+    if raw.dim() != 2:
+        raise ValueError("raw must be [B, S]")
+    B, S = raw.shape
+    dev = raw.device
+    lib = L.load()
+    cap_tok = B * S * align if tokens_capacity is None else int(tokens_capacity)
+    cap_docs = B * S + 1
+    tokens = torch.empty(max(cap_tok, 1), dtype=torch.int32, device=dev)
+    cu_v = torch.empty(cap_docs, dtype=torch.int32, device=dev)
+    cu = torch.empty(cap_docs, dtype=torch.int32, device=dev)
+    counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    ws = torch.empty(max(lib.thd_pack_docs_workspace_bytes(B), 8), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    trim = raw_pad_id is not None
+    code = lib.thd_pack_docs(_ptr(raw), B, S, int(eod_id), int(trim), int(raw_pad_id) if trim else 0, int(align),
+                             int(pad_id), _ptr(tokens), cap_tok, _ptr(cu_v), _ptr(cu), cap_docs, _ptr(counts),
+                             _ptr(ws), ws.numel(), _ptr(status), _stream(stream))
+    _raise_host(code, "thd_pack_docs")
+    check_status(status, "thd_pack_docs", stream)
+    n, T = (int(v) for v in counts.tolist())
+    return tokens[:T], cu_v[:n + 1], cu[:n + 1]
+
+
+# ---------------------------------------------------------------------------
+# the layout swap as a model layer calls it, with the route cache
+# ---------------------------------------------------------------------------
+
+class RouteCache:
+    """Reuse a built route while its source is unchanged.
+
+    Mirrors the reuse check of Relax PR #273 (sections 2.5 and the review
+    follow-up): a route is reused only for the same boundary tensor object,
+    unmodified since (its version counter), the same cp_size and the same
+    direction; anything else rebuilds.  Routes are not meant to outlive a
+    microbatch.
+    """
+
+    def __init__(self):
+        self._slots = {}
+
+    @staticmethod
+    def _key(cu, T, cp):
+        return (id(cu), cu.data_ptr(), cu._version, int(T), int(cp))
+
+    def get(self, cu, T, cp, direction, status=None, stream=None) -> Route:
+        key = self._key(cu, T, cp)
+        hit = self._slots.get(direction)
+        if hit is not None and hit[0] == key and hit[1] is cu:
+            return hit[2]
+        route = route_build(cu, T, cp, direction, status=status, stream=stream)
+        self._slots[direction] = (key, cu, route)
+        return route
+
+    def prebuild(self, cu, T, cp, status=None, stream=None):
+        """Fill both directions at once; nothing to do for cp == 1."""
+        if cp == 1:
+            return
+        for d in (ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG):
+            self.get(cu, T, cp, d, status=status, stream=stream)
+
+    def clear(self):
+        self._slots.clear()
+
+
+def zigzag_contiguous_thd_swap(x, cu_seqlens_padded, cp: int, direction: int, seq_dim: int = 0,
+                               cache: RouteCache | None = None, status=None, stream=None):
+    """Convert x between the zigzag and contiguous layouts along ``seq_dim``.
+
+    x holds all cp virtual ranks' shards of the packed sequence along seq_dim
+    (rank-major).  cp == 1 returns x itself (nothing moves), as the pages'
+    swap does.  Other dims are carried along as the row payload."""
+    if cp == 1:
+        return x
+    T = x.shape[seq_dim]
+    route = cache.get(cu_seqlens_padded, T, cp, direction, status, stream) if cache is not None else \
+        route_build(cu_seqlens_padded, T, cp, direction, status=status, stream=stream)
+    xs = x.movedim(seq_dim, 0).contiguous()
+    out = swap(xs, route, status=route.status if status is None else status, stream=stream)
+    return out.movedim(0, seq_dim)

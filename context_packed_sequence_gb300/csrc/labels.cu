@@ -1,0 +1,79 @@
+// Document-bounded labels, MTP targets and the valid-token mask.
+//
+// "Packed Sequence 与上下文并行", section 1.3 (the label roll must not cross a
+// sample), section 1.6 (MTP depth i must not take the next document's first
+// tokens as targets), section 2.2 (valid_local_token_mask is 0 on padding)
+// and section 3.8 (the EOD position's label is masked).  The pages build
+// these with an O(num_docs) Python fix-up loop and a separate MTP roll; here
+// one kernel writes every depth at once: position p of document i takes
+// tokens[p+1+k] at depth k when p+1+k is still before the document's valid
+// end e_i, else `fill` with mask 0.
+#include "thd_internal.cuh"
+
+namespace thd {
+namespace {
+
+constexpr int kLabelThreads = 512;
+constexpr int kSmemBudget = 48 * 1024;
+
+__global__ void __launch_bounds__(kLabelThreads)
+roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
+                   int32_t n, int32_t T, int32_t depth, int32_t fill, bool in_smem,
+                   int32_t* __restrict__ labels, uint8_t* __restrict__ lmask,
+                   uint8_t* __restrict__ valid, int32_t* status) {
+  extern __shared__ int32_t smem[];
+  if (block_status_set(status)) return;
+  const int32_t* cu = stage_cu(cu_g, n, smem, in_smem);
+  const int32_t* cu_v = stage_cu(cu_v_g, n, smem + (n + 1), in_smem);
+
+  int32_t code = block_check_cu(cu, n, T, 0, true);
+  if (code == THD_OK) {
+    code = block_check_cu(cu_v, n, 0, 0, false);
+    if (code == THD_OK) {
+      int bad = 0;
+      for (int32_t i = threadIdx.x; i < n; i += blockDim.x)
+        if (cu_v[i + 1] - cu_v[i] > cu[i + 1] - cu[i]) bad = 1;
+      if (__syncthreads_or(bad)) code = THD_ERR_VALID_EXCEEDS_PADDED;
+    }
+  }
+  if (code != THD_OK) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
+    return;
+  }
+
+  const int32_t stride = gridDim.x * blockDim.x;
+  for (int32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < T; p += stride) {
+    int32_t i = doc_of(cu, n, p);
+    int32_t e = cu[i] + (cu_v[i + 1] - cu_v[i]);
+    valid[p] = p < e ? 1 : 0;
+    for (int32_t k = 0; k <= depth; ++k) {
+      int32_t t = p + 1 + k;
+      bool ok = t < e;
+      labels[static_cast<int64_t>(k) * T + p] = ok ? __ldg(tokens + t) : fill;
+      lmask[static_cast<int64_t>(k) * T + p] = ok ? 1 : 0;
+    }
+  }
+}
+
+}  // namespace
+
+thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu,
+                                int32_t n, int32_t T, int32_t depth, int32_t fill, int32_t* labels,
+                                uint8_t* lmask, uint8_t* valid, int32_t* status, cudaStream_t s) {
+  size_t bytes = static_cast<size_t>(2) * (n + 1) * sizeof(int32_t);
+  bool in_smem = bytes <= static_cast<size_t>(kSmemBudget);
+  int64_t grid = (static_cast<int64_t>(T) + kLabelThreads - 1) / kLabelThreads;
+  int64_t cap = static_cast<int64_t>(sm_count()) * 2;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  roll_labels_kernel<<<static_cast<unsigned>(grid), kLabelThreads, in_smem ? bytes : 0, s>>>(
+      tokens, cu_v, cu, n, T, depth, fill, in_smem, labels, lmask, valid, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  return THD_OK;
+}
+
+}  // namespace thd

@@ -1,0 +1,98 @@
+"""The C ABI without a GPU: libthd.so loads, exports every function
+include/thd.h declares, and its host-side checks answer without touching a
+device (no compute call is made here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from context_packed_sequence_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "thd.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(thd_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from context_packed_sequence_gb300 import build
+        build.build()
+    return L.load()
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = _declared()
+    assert len(names) >= 16
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in L.SIGNATURES, f"{name} has no ctypes signature"
+    assert sorted(L.SIGNATURES) == names
+
+
+def test_status_codes_match_header(lib):
+    text = open(HEADER).read()
+    codes = dict((k, int(v)) for k, v in re.findall(r"THD_(OK|ERR_[A-Z_]+)\s*=\s*(\d+)", text))
+    assert codes["OK"] == L.OK
+    for name, val in codes.items():
+        if name != "OK":
+            assert getattr(L, name) == val, name
+    assert lib.thd_status_string(L.ERR_LEN_NOT_DIVISIBLE).decode().startswith("sequence length not divisible")
+    assert lib.thd_version() == 100
+
+
+def test_route_struct_layout():
+    assert ctypes.sizeof(L.ThdRoute) == 16 + 9 * 8
+    assert L.ThdRoute.send_rows.offset == 16
+
+
+def test_route_bytes_and_bind_host_only(lib):
+    assert lib.thd_route_bytes(24, 2) > 0
+    assert lib.thd_route_bytes(0, 4) > 0          # T = 0 is legal
+    assert lib.thd_route_bytes(26, 2) == 0        # T not a multiple of 2cp
+    assert lib.thd_route_bytes(64, 0) == 0
+    assert lib.thd_route_bytes(256, 65) == 0      # cp above the maximum
+    T, cp = 24, 2
+    nbytes = lib.thd_route_bytes(T, cp)
+    r = L.ThdRoute()
+    fake = 1 << 20  # an aligned address; bind only does arithmetic on it
+    assert lib.thd_route_bind(ctypes.byref(r), fake, nbytes, T, cp, 0) == L.OK
+    assert (r.cp_size, r.dir, r.total_rows) == (cp, 0, T)
+    ptrs = [r.send_rows, r.recv_rows, r.src_of_dst, r.input_split_sizes, r.output_split_sizes,
+            r.send_offsets, r.recv_offsets, r.send_identity, r.recv_identity]
+    assert all(p % 256 == 0 for p in ptrs)
+    assert len(set(ptrs)) == len(ptrs)
+    assert max(ptrs) < fake + nbytes
+    assert lib.thd_route_bind(ctypes.byref(r), fake, nbytes - 1, T, cp, 0) == L.ERR_INVALID_ARG
+    assert lib.thd_route_bind(ctypes.byref(r), fake + 16, nbytes, T, cp, 0) == L.ERR_INVALID_ARG
+    assert lib.thd_route_bind(ctypes.byref(r), fake, nbytes, T, cp, 7) == L.ERR_BAD_DIRECTION
+
+
+def test_host_checks_return_before_any_launch(lib):
+    r = L.ThdRoute()
+    fake = 1 << 20
+    lib.thd_route_bind(ctypes.byref(r), fake, lib.thd_route_bytes(24, 2), 24, 2, 0)
+    # direction first, then arguments -- the same order as the oracle
+    assert lib.thd_route_build(fake, 3, 24, 2, 9, ctypes.byref(r), fake, None) == L.ERR_BAD_DIRECTION
+    assert lib.thd_route_build(fake, 3, 24, 0, 0, ctypes.byref(r), fake, None) == L.ERR_INVALID_ARG
+    assert lib.thd_route_build(fake, 3, 26, 2, 0, ctypes.byref(r), fake, None) == L.ERR_INVALID_ARG
+    assert lib.thd_route_build(None, 3, 24, 2, 0, ctypes.byref(r), fake, None) == L.ERR_INVALID_ARG
+    assert lib.thd_route_build(fake, 3, 24, 2, 0, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
+    # route bound for the other direction / size
+    assert lib.thd_route_build(fake, 3, 24, 2, 1, ctypes.byref(r), fake, None) == L.ERR_INVALID_ARG
+    assert lib.thd_partition_indices(fake, 3, 24, 2, 2, fake, fake, None) == L.ERR_INVALID_ARG
+    assert lib.thd_swap(fake, fake + 8, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG  # overlap
+    assert lib.thd_swap(fake, fake + 4096, 0, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
+    assert lib.thd_swap(fake, fake + 4096, 16, None, None, None) == L.ERR_INVALID_ARG
+    assert lib.thd_roll_labels(fake, fake, fake, 3, 24, -1, 0, fake, fake, fake, fake, None) == L.ERR_INVALID_ARG
+    assert lib.thd_pack_docs(fake, 2, 8, 99, 0, 0, 0, 0, fake, 16, fake, fake, 4, fake, fake, 64, fake,
+                             None) == L.ERR_INVALID_ARG   # align 0
+    assert lib.thd_pack_docs_workspace_bytes(8) == 8 * 32
+    assert lib.thd_status_clear(None, None) == L.ERR_INVALID_ARG

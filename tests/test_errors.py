@@ -1,0 +1,165 @@
+"""Fail-fast checks on the GPU: the device status word must carry the same
+failure the oracle raises, in the same order of precedence, without any
+trap; downstream kernels must then write nothing.  Also: a corrupted route
+index is caught by the kernels' own range check, and route build plus swaps
+are captured in a CUDA graph, which any host synchronisation would break."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import thd_oracle as O
+import context_packed_sequence_gb300 as thd
+from context_packed_sequence_gb300 import _lib as L
+
+pytestmark = pytest.mark.gpu
+Z2C, C2Z = O.ZIGZAG_TO_CONTIGUOUS, O.CONTIGUOUS_TO_ZIGZAG
+
+
+def _oracle_kind(fn, *args):
+    try:
+        fn(*args)
+    except O.ThdValueError as e:
+        return e.kind
+    return "ok"
+
+
+BAD_CU = [
+    ([4, 8], 8, 2),
+    ([0, 8, 4, 8], 8, 2),
+    ([0, 6, 8], 8, 2),
+    ([0, 8], 16, 2),
+    ([4, 2, 3], 8, 2),
+    ([0, 6, 4, 9], 8, 2),
+    ([0, 6, 16], 8, 2),
+    ([0, 4, 4, 12, 10, 16], 16, 2),
+    ([0, 8, 16, 24, 30, 32], 32, 2),
+]
+
+
+@pytest.mark.parametrize("cu,T,cp", BAD_CU)
+@pytest.mark.parametrize("direction", [Z2C, C2Z])
+def test_route_status_matches_oracle(cu, T, cp, direction):
+    want = _oracle_kind(oracle.build_route, cu, T, cp, direction)
+    assert want != "ok"
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    st = thd.new_status()
+    r = thd.route_build(cu_t, T, cp, direction, status=st)
+    assert L.STATUS_NAMES[thd.status_read(st)] == want
+    # the partition kernel reports the same failure
+    st2 = thd.new_status()
+    thd.partition_indices(cu_t, T, cp, -1, status=st2)
+    assert L.STATUS_NAMES[thd.status_read(st2)] == want
+    # and a swap given the failed status writes nothing
+    x = torch.arange(T * 4, dtype=torch.int32, device="cuda").view(T, 4)
+    out = torch.full_like(x, -7)
+    thd.swap(x, r, out=out, status=st)
+    torch.cuda.synchronize()
+    assert bool((out == -7).all())
+    with pytest.raises(ValueError):
+        thd.check_status(st)
+
+
+def test_host_errors_raise_at_once():
+    cu = torch.tensor([0, 8], dtype=torch.int32, device="cuda")
+    with pytest.raises(thd.ThdError) as e:
+        thd.route_build(cu, 8, 2, 5)
+    assert e.value.kind == "bad_direction"
+    with pytest.raises(thd.ThdError) as e:
+        thd.route_build(cu, 6, 2, Z2C)
+    assert e.value.kind == "invalid_arg"
+
+
+def test_label_status_matches_oracle():
+    cases = [
+        ([1, 2, 3, 4], [0, 5], [0, 4]),
+        ([1, 2, 3, 4], [0, 2], [0, 8]),
+        ([1, 2, 3, 4], [1, 2], [0, 4]),
+        ([1, 2, 3, 4], [0, 3, 1], [0, 2, 4]),
+        ([1, 2, 3, 4], [0, 1, 2], [0, 3, 2]),
+    ]
+    for tokens, cu_v, cu in cases:
+        want = _oracle_kind(oracle.roll_labels, tokens, cu_v, cu, 1)
+        st = thd.new_status()
+        dev = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+        thd.roll_labels(dev(tokens), dev(cu_v), dev(cu), 1, status=st)
+        assert L.STATUS_NAMES[thd.status_read(st)] == want, (tokens, cu_v, cu)
+
+
+def test_status_is_sticky_until_cleared():
+    good = torch.tensor([0, 8, 16], dtype=torch.int32, device="cuda")
+    bad = torch.tensor([0, 6, 16], dtype=torch.int32, device="cuda")
+    st = thd.new_status()
+    thd.route_build(bad, 16, 2, Z2C, status=st)
+    r = thd.route_build(good, 16, 2, Z2C, status=st)      # skipped: status already set
+    assert thd.status_read(st) == L.ERR_LEN_NOT_DIVISIBLE
+    thd.status_clear(st)
+    r = thd.route_build(good, 16, 2, Z2C, status=st, route=r)
+    assert thd.status_read(st) == L.OK
+    assert r.src_of_dst.cpu().tolist() == oracle.build_route([0, 8, 16], 16, 2, Z2C).src_of_dst
+
+
+def test_corrupted_route_index_is_range_checked():
+    """An out-of-range entry is skipped by the kernel's own check (the access
+    never happens) and reported; every other row still moves."""
+    cu = [0, 8, 20, 24]
+    r = thd.route_build(torch.tensor(cu, dtype=torch.int32, device="cuda"), 24, 2, Z2C)
+    good = r.src_of_dst.clone()
+    r.src_of_dst[5] = 24 + 1000
+    r.src_of_dst[9] = -3
+    x = torch.arange(24 * 8, dtype=torch.int32, device="cuda").view(24, 8)
+    out = torch.full_like(x, -1)
+    st = thd.new_status()
+    thd.swap(x, r, out=out, status=st)
+    assert thd.status_read(st) == L.ERR_INDEX_RANGE
+    keep = [q for q in range(24) if q not in (5, 9)]
+    assert torch.equal(out[keep], x[good.long()][keep])
+    assert bool((out[5] == -1).all()) and bool((out[9] == -1).all())
+
+
+def test_route_and_swaps_capture_in_a_cuda_graph():
+    """Stream capture fails on any synchronising call, so a successful capture
+    of route build + swaps shows the path makes no host synchronisation."""
+    cu_list = [0, 8, 20, 24, 24, 64]
+    cu = torch.tensor(cu_list, dtype=torch.int32, device="cuda")
+    T, cp = 64, 4
+    x = torch.randn(T, 16, device="cuda").to(torch.bfloat16)
+    st = thd.new_status()
+    fwd = thd.Route(T, cp, Z2C)
+    bwd = thd.Route(T, cp, C2Z)
+    y = torch.empty_like(x)
+    z = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        thd.route_build(cu, T, cp, Z2C, status=st, route=fwd)      # warm-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            thd.route_build(cu, T, cp, Z2C, status=st, route=fwd)
+            thd.route_build(cu, T, cp, C2Z, status=st, route=bwd)
+            thd.swap(x, fwd, out=y, status=st)
+            thd.swap(y, bwd, out=z, status=st)
+    fwd.src_of_dst.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert thd.status_read(st) == L.OK
+    assert fwd.src_of_dst.cpu().tolist() == oracle.build_route(cu_list, T, cp, Z2C).src_of_dst
+    assert torch.equal(z, x)
+
+
+def test_python_layer_makes_no_torch_sync():
+    cu = torch.tensor([0, 16, 48], dtype=torch.int32, device="cuda")
+    x = torch.randn(48, 32, device="cuda")
+    torch.cuda.synchronize()
+    prev = torch.cuda.get_sync_debug_mode()
+    torch.cuda.set_sync_debug_mode("error")
+    try:
+        st = thd.new_status()
+        r = thd.route_build(cu, 48, 4, Z2C, status=st)
+        b = thd.route_build(cu, 48, 4, C2Z, status=st)
+        y = thd.swap(thd.swap(x, r, status=st), b, status=st)
+    finally:
+        torch.cuda.set_sync_debug_mode(prev)
+    assert torch.equal(y, x)

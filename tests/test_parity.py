@@ -1,0 +1,321 @@
+"""GPU vs oracle, element by element (integers and raw bytes: tolerance 0).
+
+Small and medium cases are compared in full; the full-size workloads compare
+the whole route exactly and the payload on sampled rows, plus the round trip
+z->c->z on every byte."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import thd_oracle as O
+import context_packed_sequence_gb300 as thd
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+Z2C, C2Z = O.ZIGZAG_TO_CONTIGUOUS, O.CONTIGUOUS_TO_ZIGZAG
+
+
+def _cu_tensor(cu):
+    return torch.tensor(cu, dtype=torch.int32, device="cuda")
+
+
+def _gpu_route(cu, T, cp, direction):
+    st = thd.new_status()
+    r = thd.route_build(_cu_tensor(cu), T, cp, direction, status=st)
+    thd.check_status(st, "route_build")
+    return r
+
+
+def _flat(list_of_lists):
+    out = []
+    for x in list_of_lists:
+        out.extend(x)
+    return out
+
+
+def _assert_route(r, o):
+    assert r.src_of_dst.cpu().tolist() == o.src_of_dst
+    assert r.send_rows.cpu().reshape(-1).tolist() == _flat(o.send_rows)
+    assert r.recv_rows.cpu().reshape(-1).tolist() == _flat(o.recv_rows)
+    assert r.input_split_sizes.cpu().tolist() == o.input_split_sizes
+    assert r.output_split_sizes.cpu().tolist() == o.output_split_sizes
+    assert r.send_offsets.cpu().tolist() == o.send_offsets
+    assert r.recv_offsets.cpu().tolist() == o.recv_offsets
+    assert [bool(v) for v in r.send_identity.cpu().tolist()] == o.send_identity
+    assert [bool(v) for v in r.recv_identity.cpu().tolist()] == o.recv_identity
+
+
+def _bounds(lengths):
+    return W.boundaries(lengths)
+
+
+# --------------------------------------------------------------------------
+# route and partition
+# --------------------------------------------------------------------------
+
+def test_tiny_workload_route_and_partition():
+    lens = W.doc_lengths("tiny")
+    cu, cp = _bounds(lens), 2
+    T = cu[-1]
+    for d in (Z2C, C2Z):
+        _assert_route(_gpu_route(cu, T, cp, d), oracle.build_route(cu, T, cp, d))
+    st = thd.new_status()
+    allr = thd.partition_indices(_cu_tensor(cu), T, cp, -1, status=st)
+    one = [thd.partition_indices(_cu_tensor(cu), T, cp, r, status=st) for r in range(cp)]
+    thd.check_status(st)
+    assert allr.cpu().reshape(-1).tolist() == oracle.partition_indices(cu, T, cp, -1)
+    for r in range(cp):
+        assert one[r].cpu().tolist() == oracle.partition_indices(cu, T, cp, r)
+
+
+def _small_packings():
+    import itertools
+    for cp in (1, 2, 3, 4):
+        unit, max_units = 2 * cp, 24 // (2 * cp)
+        yield cp, []
+        for n in range(1, 4):
+            for parts in itertools.product(range(max_units + 1), repeat=n):
+                if sum(parts) <= max_units:
+                    yield cp, [unit * p for p in parts]
+
+
+def test_route_bruteforce_small_packings():
+    n = 0
+    for cp, lens in _small_packings():
+        cu = _bounds(lens)
+        T = cu[-1]
+        for d in (Z2C, C2Z):
+            _assert_route(_gpu_route(cu, T, cp, d), oracle.build_route(cu, T, cp, d))
+            n += 1
+    assert n > 500
+
+
+MEDIUM = [
+    # (seed, cp, n_docs, max_chunk, empty_frac)
+    (1, 2, 40, 64, 0.1),
+    (2, 3, 120, 20, 0.2),
+    (3, 4, 300, 12, 0.0),
+    (4, 5, 17, 300, 0.3),
+    (5, 8, 200, 9, 0.1),
+    (6, 16, 150, 5, 0.05),
+    (7, 64, 30, 3, 0.0),
+    (8, 7, 1, 2000, 0.0),          # one long document
+]
+
+
+@pytest.mark.parametrize("seed,cp,n_docs,max_chunk,empty", MEDIUM)
+def test_route_medium(seed, cp, n_docs, max_chunk, empty):
+    lens = W.random_lengths(seed, n_docs, cp, max_chunk, empty)
+    cu = _bounds(lens)
+    T = cu[-1]
+    for d in (Z2C, C2Z):
+        _assert_route(_gpu_route(cu, T, cp, d), oracle.build_route(cu, T, cp, d))
+    st = thd.new_status()
+    got = thd.partition_indices(_cu_tensor(cu), T, cp, -1, status=st)
+    thd.check_status(st)
+    assert got.cpu().reshape(-1).tolist() == oracle.partition_indices(cu, T, cp, -1)
+
+
+@pytest.mark.parametrize("cp,n_docs", [(2, 13000), (64, 4000)])
+def test_route_boundaries_beyond_shared_memory(cp, n_docs):
+    """Enough documents that the boundaries are searched in global memory."""
+    lens = W.random_lengths(99 + cp, n_docs, cp, 2, 0.1)
+    cu = _bounds(lens)
+    T = cu[-1]
+    for d in (Z2C, C2Z):
+        _assert_route(_gpu_route(cu, T, cp, d), oracle.build_route(cu, T, cp, d))
+
+
+def test_empty_packing_and_cp1():
+    for cu in ([0], [0, 0, 0]):
+        for d in (Z2C, C2Z):
+            _assert_route(_gpu_route(cu, 0, 4, d), oracle.build_route(cu, 0, 4, d))
+    cu = _bounds([2, 6, 0, 10])
+    for d in (Z2C, C2Z):
+        r = _gpu_route(cu, 18, 1, d)
+        _assert_route(r, oracle.build_route(cu, 18, 1, d))
+        assert r.src_of_dst.cpu().tolist() == list(range(18))
+
+
+# --------------------------------------------------------------------------
+# payload movement: fused swap and the three steps, every copy-unit width
+# --------------------------------------------------------------------------
+
+def _payload(seed, T, row_bytes):
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, 256, size=(T, row_bytes), dtype=np.uint8)
+
+
+@pytest.mark.parametrize("row_bytes", [1, 2, 6, 12, 16, 48, 512, 4096])
+@pytest.mark.parametrize("seed,cp,n_docs,max_chunk,empty", [MEDIUM[1], MEDIUM[4], (11, 4, 9, 7, 0.2)])
+def test_apply_parity(row_bytes, seed, cp, n_docs, max_chunk, empty):
+    lens = W.random_lengths(seed, n_docs, cp, max_chunk, empty)
+    cu = _bounds(lens)
+    T = cu[-1]
+    if T * row_bytes > 64 << 20:
+        pytest.skip("kept small for the CPU oracle")
+    x_np = _payload(seed * 31 + row_bytes, T, row_bytes)
+    x = torch.from_numpy(x_np).cuda()
+    for d in (Z2C, C2Z):
+        o = oracle.build_route(cu, T, cp, d)
+        send_o, recv_o, out_o = oracle.apply_route(x_np, o)
+        r = _gpu_route(cu, T, cp, d)
+        st = thd.new_status()
+        out = thd.swap(x, r, status=st)
+        send = thd.pack(x, r, status=st)
+        recv = thd.a2a_local(send, r, status=st)
+        out3 = thd.scatter(recv, r, status=st)
+        thd.check_status(st)
+        assert np.array_equal(out.cpu().numpy(), out_o)
+        assert np.array_equal(send.cpu().numpy(), send_o)
+        assert np.array_equal(recv.cpu().numpy(), recv_o)
+        assert np.array_equal(out3.cpu().numpy(), out_o)
+
+
+def test_tiny_workload_payloads():
+    """x bf16 [24, 2, 4] and int32 ids, z->c and back, bit for bit."""
+    w = W.BY_NAME["tiny"]
+    cu = _bounds(W.doc_lengths("tiny"))
+    T = cu[-1]
+    x = W.payload_host(w.seed, T, w.hidden)
+    ids = torch.from_numpy(W.token_ids(w.seed, T)).view(T, 1)
+    for t in (x, ids):
+        raw = t.contiguous().view(torch.uint8).reshape(T, -1).numpy()
+        fwd = oracle.build_route(cu, T, 2, Z2C)
+        _, _, want = oracle.apply_route(raw, fwd)
+        r = _gpu_route(cu, T, 2, Z2C)
+        b = _gpu_route(cu, T, 2, C2Z)
+        got = thd.swap(t.cuda(), r)
+        back = thd.swap(got, b)
+        assert np.array_equal(got.cpu().contiguous().view(torch.uint8).reshape(T, -1).numpy(), want)
+        assert torch.equal(back.cpu(), t)
+
+
+def test_guard_rows_untouched():
+    cu = _bounds(W.random_lengths(5, 50, 4, 9, 0.1))
+    T = cu[-1]
+    r = _gpu_route(cu, T, 4, Z2C)
+    x = torch.randint(0, 255, (T, 64), dtype=torch.uint8, device="cuda")
+    big = torch.full((T + 64, 64), 0xA5, dtype=torch.uint8, device="cuda")
+    out = big[32:32 + T]
+    thd.swap(x, r, out=out)
+    torch.cuda.synchronize()
+    assert bool((big[:32] == 0xA5).all()) and bool((big[32 + T:] == 0xA5).all())
+    assert torch.equal(out, x[r.src_of_dst.long()])
+
+
+def test_movedim_wrapper_and_cache():
+    cu = _cu_tensor(_bounds(W.random_lengths(3, 20, 2, 6, 0.0)))
+    T = int(cu[-1])
+    x = torch.randn(3, T, 8, device="cuda").to(torch.bfloat16)   # sequence on dim 1
+    cache = thd.RouteCache()
+    y = thd.zigzag_contiguous_thd_swap(x, cu, 2, thd.ZIGZAG_TO_CONTIGUOUS, seq_dim=1, cache=cache)
+    z = thd.zigzag_contiguous_thd_swap(y, cu, 2, thd.CONTIGUOUS_TO_ZIGZAG, seq_dim=1, cache=cache)
+    assert torch.equal(z, x)
+    o = oracle.build_route(cu.cpu().tolist(), T, 2, Z2C)
+    assert torch.equal(y, x[:, torch.tensor(o.src_of_dst, device="cuda").long()])
+    r1 = cache.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS)
+    assert cache.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is r1          # same object: hit
+    assert cache.get(cu, T, 2, thd.CONTIGUOUS_TO_ZIGZAG) is not r1      # directions apart
+    cu.add_(0)                                                          # in-place write bumps _version
+    assert cache.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is not r1
+    assert cache.get(cu.clone(), T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is not r1
+    assert thd.zigzag_contiguous_thd_swap(x, cu, 1, 0, seq_dim=1) is x  # cp == 1: nothing moves
+
+
+# --------------------------------------------------------------------------
+# labels and packing
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("depth", [0, 1, 3])
+def test_roll_labels_parity(depth):
+    rng = np.random.default_rng(40 + depth)
+    for trial in range(12):
+        n = int(rng.integers(0, 60))
+        lv = [int(rng.integers(0, 40)) for _ in range(n)]
+        lp = [L + int(rng.integers(0, 17)) for L in lv]
+        cu_v, cu = _bounds(lv), _bounds(lp)
+        T = cu[-1]
+        tokens = [int(t) for t in rng.integers(0, 151936, size=T)]
+        want = oracle.roll_labels(tokens, cu_v, cu, depth, fill=-100)
+        st = thd.new_status()
+        got = thd.roll_labels(torch.tensor(tokens, dtype=torch.int32, device="cuda"), _cu_tensor(cu_v),
+                              _cu_tensor(cu), depth, -100, status=st)
+        thd.check_status(st)
+        assert got[0].cpu().tolist() == want[0]
+        assert got[1].cpu().tolist() == want[1]
+        assert got[2].cpu().tolist() == want[2]
+
+
+def test_pack_docs_worked_example_and_corners():
+    E = 99
+    cases = [
+        ([[1, 2, 3, E, 4, 5, E, 0], [6, 7, 8, 9, 10, E, 0, 0]], 4, 0),
+        ([[0, 0, 0, 0], [1, 2, E, 3], [1, 2, 3, E], [E, E, 5, 6], [7, 8, 9, 9], [4, 0, E, 0]], 4, 0),
+        ([[0, 0, 0]], 4, 0),
+    ]
+    for raw, align, rp in cases:
+        want = oracle.pack_docs(raw, E, align, pad_id=77, raw_pad_id=rp)
+        got = thd.pack_docs(torch.tensor(raw, dtype=torch.int32, device="cuda"), E, align, pad_id=77,
+                            raw_pad_id=rp)
+        assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
+
+
+def test_pack_docs_random_against_oracle():
+    rng = np.random.default_rng(8)
+    for trial in range(10):
+        B, S = int(rng.integers(1, 6)), int(rng.integers(1, 20000))
+        raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+        raw[rng.random((B, S)) < float(rng.choice([0.0005, 0.01, 0.3]))] = 7
+        align = int(rng.choice([1, 4, 16]))
+        want = oracle.pack_docs(raw.tolist(), 7, align, pad_id=0)
+        got = thd.pack_docs(torch.from_numpy(raw).cuda(), 7, align, pad_id=0)
+        assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
+
+
+# --------------------------------------------------------------------------
+# the full-size workloads, in the launch configuration the benchmark times
+# --------------------------------------------------------------------------
+
+def _full_size_swap_check(cu, cp, hidden, seed, sample=4096):
+    T = cu[-1]
+    x = W.payload_device(seed, T, hidden, "cuda")
+    for d in (Z2C, C2Z):
+        o = oracle.build_route(cu, T, cp, d)
+        r = _gpu_route(cu, T, cp, d)
+        _assert_route(r, o)
+        st = thd.new_status()
+        out = thd.swap(x, r, status=st)
+        thd.check_status(st)
+        rows = np.random.default_rng(seed + d).integers(0, T, size=sample)
+        src = torch.tensor([o.src_of_dst[q] for q in rows], device="cuda").long()
+        assert torch.equal(out[torch.from_numpy(rows).cuda().long()], x[src])
+        if d == Z2C:
+            fwd = out
+    back = thd.swap(fwd, _gpu_route(cu, T, cp, C2Z))
+    assert torch.equal(back, x)
+
+
+@pytest.mark.parametrize("name", ["lognorm128k", "longtail128k", "stress16"])
+def test_full_size_workloads(name):
+    w = W.BY_NAME[name]
+    cu = _bounds(W.doc_lengths(name))
+    _full_size_swap_check(cu, w.cp, w.hidden, w.seed)
+
+
+def test_full_size_pipeline():
+    w = W.BY_NAME["pipeline"]
+    raw = W.raw_pipeline_tokens(w.seed)
+    tok_o, cu_v_o, cu_o = oracle.pack_docs(raw.tolist(), W.EOD_ID, 2 * w.cp, pad_id=0)
+    tok, cu_v, cu = thd.pack_docs(torch.from_numpy(raw).cuda(), W.EOD_ID, 2 * w.cp, pad_id=0)
+    assert tok.cpu().tolist() == tok_o
+    assert cu_v.cpu().tolist() == cu_v_o
+    assert cu.cpu().tolist() == cu_o
+    labels, lmask, valid = thd.roll_labels(tok, cu_v, cu, w.mtp_depth, fill=0)
+    lab_o, msk_o, val_o = oracle.roll_labels(tok_o, cu_v_o, cu_o, w.mtp_depth, fill=0)
+    assert labels.cpu().tolist() == lab_o
+    assert lmask.cpu().tolist() == msk_o
+    assert valid.cpu().tolist() == val_o
+    _full_size_swap_check(cu_o, w.cp, w.hidden, w.seed, sample=2048)
