@@ -123,7 +123,7 @@ def measured_peak():
 def swap_traffic_record():
     """dram bytes per swap launch from the committed ncu summary, or None when
     the summary is missing or the copy kernel's source changed since."""
-    path = os.path.join(ROOT, "profiles", "copy_rows_swap_lognorm128k.md")
+    path = os.path.join(ROOT, "profiles", "bulk_copy_swap_lognorm128k.md")
     src = os.path.join(ROOT, "context_packed_sequence_gb300", "csrc", "copy.cu")
     try:
         text = open(path).read()
@@ -141,6 +141,14 @@ def swap_traffic_record():
         return int(fields["dram bytes per launch"])
     except (KeyError, ValueError):
         return None
+
+
+def plan_kernel_name(row_bytes: int) -> str:
+    """The kernel thd_swap launches for this row size (see the bulk plan in copy.cu)."""
+    if row_bytes % 16 or row_bytes < 256:
+        return "copy_rows_kernel<unit, SwapMap, false> (thd_swap)"
+    nst = 2 if row_bytes <= 8192 else (4 if row_bytes <= 16384 else (3 if row_bytes <= 32768 else 4))
+    return f"bulk_copy_kernel<{nst}, SwapMap, false> (thd_swap)"
 
 
 class ClockSampler:
@@ -375,13 +383,13 @@ def run_thd(args, rank, world, local):
         "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": "copy_rows_kernel<uint4, SwapMap> (thd_swap)",
+            "kernel": plan_kernel_name(row_bytes),
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth (read+write)",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic,
+            "traffic": traffic if w.name == "lognorm128k" else None,
             "algorithmic_bytes_per_launch": swap_bytes,
         },
         "gpu_launches": launches_per_step * n_ev,

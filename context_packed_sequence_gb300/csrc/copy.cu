@@ -2,15 +2,21 @@
 // (pack -> all-to-all -> scatter, "[Task32] feat: fla mcore chunkwise cp
 // stage 3", Relax PR #273, section 2.1) with every virtual rank in one buffer.
 //
-// Pure data movement, bound by HBM bandwidth.  One engine serves all four:
-// the "linear" side (the destination of a gather, the source of a scatter) is
-// walked as one flat array of copy units (16, 4 or 1 bytes); each warp takes
-// 32*U consecutive units per step, so linear-side accesses are 512-byte
-// coalesced runs for 16-byte units, and the mapped side reads or writes
-// contiguous pieces of whole rows.  Each lane keeps (row, column) of its units
-// incrementally -- no division inside the loop -- and resolves a row's partner
-// once per row change.  Every partner row is range-checked; a bad one is
-// skipped and reported through the status word.
+// Pure data movement, bound by HBM bandwidth.  Two engines, one row map each
+// call (linear-side row -> mapped-side row, range-checked):
+//
+//  * bulk engine (rows of >= 256 bytes, multiples of 16, 16-byte aligned
+//    buffers): one warp per block drives a ring of shared-memory stages with
+//    TMA bulk copies.  The linear side is cut into chunks of up to 32 rows
+//    (or row pieces); each chunk is gathered with one cp.async.bulk
+//    global->shared copy per run of consecutive mapped rows, completion
+//    tracked by an mbarrier, and written back with one bulk store per run.
+//    The SM issues a handful of instructions per 8-16 KB moved, so the copy
+//    runs at the HBM copy rate.  Every wait is bounded: a wait that runs out
+//    records THD_ERR_TIMEOUT, drains its own copies and returns.
+//  * unit engine (everything else: narrow, odd-sized or unaligned rows): the
+//    linear side is walked as a flat array of 16-, 4- or 1-byte units, 32*U
+//    consecutive units per warp step, (row, column) kept incrementally.
 #include "thd_internal.cuh"
 
 namespace thd {
@@ -19,6 +25,7 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kUnroll = 8;
 constexpr int kCopyBlocksPerSm = 3;
+constexpr int64_t kBulkMinRowBytes = 256;  // narrower rows: the unit engine
 
 // ---- memory access flavours ------------------------------------------------
 
@@ -89,7 +96,7 @@ struct A2AMap {
   }
 };
 
-// ---- the engine ------------------------------------------------------------
+// ---- the unit engine -------------------------------------------------------
 
 struct Walk {
   int32_t rows;    // rows on the linear side
@@ -194,10 +201,287 @@ thd_status_t run(const void* src, void* dst, int32_t rows, int64_t row_bytes, Ma
   return THD_OK;
 }
 
+
+// ---- the bulk (TMA) engine -------------------------------------------------
+
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kWaitLimit = 1 << 20;  // try_wait polls before a wait gives up
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+// Bounded wait for the phase with the given parity; false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (int it = 0; it < kWaitLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(sdst)),
+               "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// all but the newest bulk group of this thread have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Lane `lane` starts a run in `starts`; the run ends before the next lane that
+// starts another run or is not in `members`.
+__device__ __forceinline__ int run_end(int lane, uint32_t starts, uint32_t members) {
+  const uint32_t above = lane == 31 ? 0u : ~((2u << lane) - 1u);
+  const uint32_t stop = (starts | ~members) & above;
+  return stop ? __ffs(stop) - 1 : 32;
+}
+
+struct BulkGeom {
+  int32_t rows;       // rows on either side
+  int32_t row_bytes;
+  int32_t stage;      // bytes per stage
+  int32_t R;          // rows per chunk (row mode) or 1
+  int32_t P;          // pieces per row (piece mode) or 1
+  int64_t chunks;
+};
+
+// Shared memory: NST stages, then NST mbarriers, NST valid masks, NST x 32 mapped rows.
+template <int NST, class Map, bool SCATTER>
+__global__ void __launch_bounds__(32)
+bulk_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, BulkGeom g, Map map, int32_t* status) {
+  extern __shared__ __align__(128) char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(NST) * g.stage);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(bars + NST);
+  int32_t* mrows = reinterpret_cast<int32_t*>(masks + NST);
+  const int lane = threadIdx.x;
+  // one read, broadcast: the warp must take this exit together
+  if (__shfl_sync(kFull, lane == 0 ? status_load(status) : 0, 0) != 0) return;
+  const int64_t b = blockIdx.x, G = gridDim.x;
+  const int64_t n_my = g.chunks > b ? (g.chunks - b + G - 1) / G : 0;
+  if (n_my == 0) return;
+  const bool row_mode = g.P == 1;
+  const int64_t rb = g.row_bytes;
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  bool bad = false;
+
+  // mapped row of this lane's row of chunk i (-1: out of range, -2: no row)
+  auto fetch = [&](int64_t i) -> int32_t {
+    const int64_t k = b + i * G;
+    const int64_t q = row_mode ? k * g.R + lane : k / g.P;
+    if (row_mode && (lane >= g.R || q >= g.rows)) return -2;
+    return map(static_cast<int32_t>(q));
+  };
+
+  auto issue_load = [&](int64_t i, int32_t m) {
+    const int s = static_cast<int>(i % NST);
+    char* st = smem + static_cast<size_t>(s) * g.stage;
+    const int64_t k = b + i * G;
+    bad |= (m == -1);
+    if (row_mode) {
+      const int64_t q0 = k * g.R;
+      const bool valid = m >= 0;
+      const uint32_t vmask = __ballot_sync(kFull, valid);
+      bool start;
+      if (SCATTER) {  // contiguous linear source: runs of valid rows
+        start = valid && (lane == 0 || !((vmask >> (lane - 1)) & 1u));
+      } else {        // gather: runs of consecutive mapped rows
+        const int32_t pm = __shfl_up_sync(kFull, m, 1);
+        start = valid && (lane == 0 || pm < 0 || m != pm + 1);
+      }
+      const uint32_t smask = __ballot_sync(kFull, start);
+      mrows[s * 32 + lane] = m;
+      if (lane == 0) {
+        masks[s] = vmask;
+        mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(__popc(vmask)) * static_cast<uint32_t>(rb));
+      }
+      __syncwarp();
+      if (start) {
+        const int end = run_end(lane, smask, vmask);
+        const char* from = SCATTER ? src + (q0 + lane) * rb : src + static_cast<int64_t>(m) * rb;
+        bulk_load(st + lane * rb, from, static_cast<uint32_t>((end - lane) * rb), &bars[s]);
+      }
+    } else if (lane == 0) {
+      const int64_t q = k / g.P;
+      const int64_t off = (k % g.P) * g.stage;
+      const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(g.stage), rb - off));
+      masks[s] = m >= 0 ? 1u : 0u;
+      mrows[s * 32] = m;
+      if (m >= 0) {
+        mbar_arrive_expect_tx(&bars[s], bytes);
+        const char* from = SCATTER ? src + q * rb + off : src + static_cast<int64_t>(m) * rb + off;
+        bulk_load(st, from, bytes, &bars[s]);
+      } else {
+        mbar_arrive_expect_tx(&bars[s], 0);
+      }
+    }
+    __syncwarp();
+  };
+
+  auto issue_store = [&](int64_t i) {
+    const int s = static_cast<int>(i % NST);
+    const char* st = smem + static_cast<size_t>(s) * g.stage;
+    const int64_t k = b + i * G;
+    const uint32_t vmask = masks[s];
+    if (row_mode) {
+      const int64_t q0 = k * g.R;
+      const int32_t m = mrows[s * 32 + lane];
+      const bool valid = (vmask >> lane) & 1u;
+      bool start;
+      if (SCATTER) {  // runs of consecutive mapped rows
+        const int32_t pm = __shfl_up_sync(kFull, m, 1);
+        start = valid && (lane == 0 || pm < 0 || m != pm + 1);
+      } else {        // contiguous linear destination: runs of valid rows
+        start = valid && (lane == 0 || !((vmask >> (lane - 1)) & 1u));
+      }
+      const uint32_t smask = __ballot_sync(kFull, start);
+      if (start) {
+        const int end = run_end(lane, smask, vmask);
+        char* to = SCATTER ? dst + static_cast<int64_t>(m) * rb : dst + (q0 + lane) * rb;
+        bulk_store(to, st + lane * rb, static_cast<uint32_t>((end - lane) * rb));
+      }
+    } else if (lane == 0 && vmask) {
+      const int64_t q = k / g.P;
+      const int64_t off = (k % g.P) * g.stage;
+      const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(g.stage), rb - off));
+      const int32_t m = mrows[s * 32];
+      char* to = SCATTER ? dst + static_cast<int64_t>(m) * rb + off : dst + q * rb + off;
+      bulk_store(to, st, bytes);
+    }
+    bulk_commit();
+  };
+
+  // Loads run NST-1 chunks ahead of stores.  The mapped rows of the chunk to
+  // be loaded next are fetched before waiting, so their latency overlaps.
+  int64_t issued = 0;
+  for (; issued < NST - 1 && issued < n_my; ++issued) issue_load(issued, fetch(issued));
+  bool timed_out = false;
+  int64_t i = 0;
+  for (; i < n_my; ++i) {
+    const int64_t j = i + NST - 1;
+    const int32_t mj = j < n_my ? fetch(j) : -2;
+    const bool landed = mbar_wait(&bars[i % NST], static_cast<uint32_t>((i / NST) & 1));
+    if (!__all_sync(kFull, landed)) {  // give up together, never with part of the warp
+      timed_out = true;
+      break;
+    }
+    issue_store(i);
+    if (j < n_my) {
+      bulk_wait_read_all_but_one();  // the store that used stage j % NST is done reading it
+      __syncwarp();
+      issue_load(j, mj);
+      issued = j + 1;
+    }
+  }
+  if (timed_out) {
+    // let this block's copies in flight land before shared memory goes away
+    for (int64_t r = i; r < issued; ++r) mbar_wait(&bars[r % NST], static_cast<uint32_t>((r / NST) & 1));
+    if (lane == 0) status_set(status, THD_ERR_TIMEOUT);
+  }
+  bulk_wait_all();
+  if (bad) status_set(status, THD_ERR_INDEX_RANGE);
+}
+
+// Stage size, ring depth and blocks per SM by row size (chosen by a sweep on
+// GB300 over 4 KiB - 48 KiB stages, 2-8 stages, 1-8 blocks per SM):
+//   rows <= 8 KiB : chunks of up to 8 KiB (R rows), 2 stages, 6 blocks per SM
+//   rows <= 16 KiB: one row per chunk, 4 stages, 3 blocks per SM
+//   rows <= 32 KiB: one row per chunk, 3 stages, 2 blocks per SM
+//   larger rows   : 16 KiB pieces, 4 stages, 3 blocks per SM
+struct BulkPlan {
+  int nst, cps;
+  BulkGeom g;
+};
+
+BulkPlan bulk_plan(int32_t rows, int64_t row_bytes) {
+  BulkPlan p;
+  p.g.rows = rows;
+  p.g.row_bytes = static_cast<int32_t>(row_bytes);
+  if (row_bytes <= 8192) {
+    p.g.R = static_cast<int32_t>(8192 / row_bytes < 32 ? 8192 / row_bytes : 32);
+    p.g.P = 1;
+    p.g.stage = static_cast<int32_t>(p.g.R * row_bytes);
+    p.nst = 2;
+    p.cps = 6;
+  } else if (row_bytes <= 32768) {
+    p.g.R = 1;
+    p.g.P = 1;
+    p.g.stage = static_cast<int32_t>(row_bytes);
+    p.nst = row_bytes <= 16384 ? 4 : 3;
+    p.cps = row_bytes <= 16384 ? 3 : 2;
+  } else {
+    p.g.R = 1;
+    p.g.stage = 16384;
+    p.g.P = static_cast<int32_t>((row_bytes + p.g.stage - 1) / p.g.stage);
+    p.nst = 4;
+    p.cps = 3;
+  }
+  p.g.chunks = p.g.P == 1 ? (static_cast<int64_t>(rows) + p.g.R - 1) / p.g.R : static_cast<int64_t>(rows) * p.g.P;
+  return p;
+}
+
+template <int NST, class Map, bool SCATTER>
+thd_status_t launch_bulk(const BulkPlan& p, const void* src, void* dst, Map map, int32_t* status, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(NST) * p.g.stage + NST * (8 + 4 + 32 * 4);
+  cudaError_t e = cudaSuccess;
+  if (smem > 48 * 1024)
+    e = cudaFuncSetAttribute(bulk_copy_kernel<NST, Map, SCATTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (e == cudaSuccess) {
+    int64_t grid = static_cast<int64_t>(sm_count()) * p.cps;
+    if (grid > p.g.chunks) grid = p.g.chunks;
+    if (grid < 1) grid = 1;
+    bulk_copy_kernel<NST, Map, SCATTER><<<static_cast<unsigned>(grid), 32, smem, s>>>(
+        static_cast<const char*>(src), static_cast<char*>(dst), p.g, map, status);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  return THD_OK;
+}
+
+template <class Map, bool SCATTER>
+thd_status_t run_bulk(const void* src, void* dst, int32_t rows, int64_t row_bytes, Map map, int32_t* status,
+                      cudaStream_t s) {
+  const BulkPlan p = bulk_plan(rows, row_bytes);
+  switch (p.nst) {
+    case 2: return launch_bulk<2, Map, SCATTER>(p, src, dst, map, status, s);
+    case 3: return launch_bulk<3, Map, SCATTER>(p, src, dst, map, status, s);
+    default: return launch_bulk<4, Map, SCATTER>(p, src, dst, map, status, s);
+  }
+}
+
 template <class Map, bool SCATTER>
 thd_status_t dispatch_unit(const void* src, void* dst, int32_t rows, int64_t row_bytes, Map map,
                            int32_t* status, cudaStream_t s) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+  if (row_bytes % 16 == 0 && a % 16 == 0 && row_bytes >= kBulkMinRowBytes)
+    return run_bulk<Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
   if (row_bytes % 16 == 0 && a % 16 == 0)
     return run<uint4, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
   if (row_bytes % 4 == 0 && a % 4 == 0)

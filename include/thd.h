@@ -31,7 +31,9 @@
  *    caller's status word `d_status` (device int32, clear it to 0 before
  *    first use).  The first error wins; a kernel that finds *d_status != 0
  *    on entry writes nothing, so one bad microbatch cannot scribble over
- *    memory downstream.  No kernel traps, asserts or spins.
+ *    memory downstream.  No kernel traps or asserts; the only waits (copy
+ *    completion in the bulk copy pipeline) are bounded and report
+ *    THD_ERR_TIMEOUT when they give up.
  *  - Every row index a kernel computes or reads is checked against its
  *    buffer before use; a bad one is skipped and reported as
  *    THD_ERR_INDEX_RANGE.
@@ -56,7 +58,7 @@ typedef enum thd_status {
   THD_ERR_CU_NON_MONOTONE = 4,       /* device: cu[i+1] < cu[i] for some i */
   THD_ERR_LEN_NOT_DIVISIBLE = 5,     /* device: a padded length is not a multiple of 2*cp */
   THD_ERR_TOTAL_MISMATCH = 6,        /* device: cu[num_docs] != T */
-  THD_ERR_TIMEOUT = 7,               /* reserved: no kernel of this library waits on anything */
+  THD_ERR_TIMEOUT = 7,               /* device: a bounded wait in the bulk copy pipeline gave up */
   THD_ERR_CUDA = 8,                  /* host: a CUDA call failed, see thd_last_cuda_error() */
   THD_ERR_INDEX_RANGE = 9,           /* device: a route index was outside its buffer */
   THD_ERR_VALID_EXCEEDS_PADDED = 10, /* device: an unpadded length exceeds its padded length */
@@ -157,8 +159,9 @@ thd_status_t thd_partition_indices(const int32_t *cu_seqlens_padded, int32_t num
  * `row_bytes` bytes (Relax PR #273, section 2.1: pack -> all-to-all ->
  * scatter, here one pass that reads and writes every row once).
  *  src, dst   device buffers of T*row_bytes bytes that must not overlap.
- *  row_bytes  > 0; a multiple of 16 with 16-byte aligned src/dst takes the
- *             16-byte vector path, else 4-byte, else 1-byte.
+ *  row_bytes  > 0.  Rows of >= 256 bytes that are a multiple of 16, with
+ *             16-byte aligned src/dst, move by TMA bulk copies through
+ *             shared memory; other rows by 16-, 4- or 1-byte loads/stores.
  *  d_status   device int32[1] or NULL.  When given, the swap does nothing if
  *             it is non-zero on entry, and records THD_ERR_INDEX_RANGE.
  */

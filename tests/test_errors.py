@@ -100,15 +100,18 @@ def test_status_is_sticky_until_cleared():
     assert r.src_of_dst.cpu().tolist() == oracle.build_route([0, 8, 16], 16, 2, Z2C).src_of_dst
 
 
-def test_corrupted_route_index_is_range_checked():
+@pytest.mark.parametrize("width", [8, 128, 4096, 12288])
+def test_corrupted_route_index_is_range_checked(width):
     """An out-of-range entry is skipped by the kernel's own check (the access
-    never happens) and reported; every other row still moves."""
+    never happens) and reported; every other row still moves.  Widths cover
+    the unit engine (32 B rows) and the bulk engine (512 B, 16 KiB rows and
+    48 KiB rows cut into pieces)."""
     cu = [0, 8, 20, 24]
     r = thd.route_build(torch.tensor(cu, dtype=torch.int32, device="cuda"), 24, 2, Z2C)
     good = r.src_of_dst.clone()
     r.src_of_dst[5] = 24 + 1000
     r.src_of_dst[9] = -3
-    x = torch.arange(24 * 8, dtype=torch.int32, device="cuda").view(24, 8)
+    x = torch.arange(24 * width, dtype=torch.int32, device="cuda").view(24, width)
     out = torch.full_like(x, -1)
     st = thd.new_status()
     thd.swap(x, r, out=out, status=st)
@@ -121,9 +124,9 @@ def test_corrupted_route_index_is_range_checked():
 def test_route_and_swaps_capture_in_a_cuda_graph():
     """Stream capture fails on any synchronising call, so a successful capture
     of route build + swaps shows the path makes no host synchronisation."""
-    cu_list = [0, 8, 20, 24, 24, 64]
+    cu_list = [0, 8, 20, 24, 24, 64]          # lengths 8, 12, 4, 0, 40: multiples of 2*cp
     cu = torch.tensor(cu_list, dtype=torch.int32, device="cuda")
-    T, cp = 64, 4
+    T, cp = 64, 2
     x = torch.randn(T, 16, device="cuda").to(torch.bfloat16)
     st = thd.new_status()
     fwd = thd.Route(T, cp, Z2C)

@@ -174,6 +174,48 @@ def test_apply_parity(row_bytes, seed, cp, n_docs, max_chunk, empty):
         assert np.array_equal(out3.cpu().numpy(), out_o)
 
 
+@pytest.mark.parametrize("row_bytes", [256, 8192, 10240, 20480, 40960])
+def test_apply_parity_wide_rows(row_bytes):
+    """Every plan of the bulk engine: 32 rows per chunk, one row per chunk with
+    2/4/3 stages, and rows cut into 16 KiB pieces."""
+    for seed, cp, n_docs, max_chunk, empty in [(21, 2, 30, 6, 0.1), (22, 4, 9, 5, 0.2)]:
+        lens = W.random_lengths(seed, n_docs, cp, max_chunk, empty)
+        cu = _bounds(lens)
+        T = cu[-1]
+        x_np = _payload(seed * 7 + row_bytes, T, row_bytes)
+        x = torch.from_numpy(x_np).cuda()
+        for d in (Z2C, C2Z):
+            o = oracle.build_route(cu, T, cp, d)
+            send_o, recv_o, out_o = oracle.apply_route(x_np, o)
+            r = _gpu_route(cu, T, cp, d)
+            st = thd.new_status()
+            out = thd.swap(x, r, status=st)
+            send = thd.pack(x, r, status=st)
+            recv = thd.a2a_local(send, r, status=st)
+            out3 = thd.scatter(recv, r, status=st)
+            thd.check_status(st)
+            assert np.array_equal(out.cpu().numpy(), out_o)
+            assert np.array_equal(send.cpu().numpy(), send_o)
+            assert np.array_equal(recv.cpu().numpy(), recv_o)
+            assert np.array_equal(out3.cpu().numpy(), out_o)
+
+
+def test_unaligned_buffers_take_the_narrow_path():
+    """16-byte-multiple rows at a 4-byte offset: correct through the 4-byte units."""
+    cu = _bounds(W.random_lengths(31, 25, 2, 9, 0.1))
+    T, rb = cu[-1], 512
+    x_np = _payload(5, T, rb)
+    base = torch.zeros(T * rb + 4, dtype=torch.uint8, device="cuda")
+    x = base[4:].view(T, rb)
+    x.copy_(torch.from_numpy(x_np))
+    obase = torch.zeros(T * rb + 4, dtype=torch.uint8, device="cuda")
+    out = obase[4:].view(T, rb)
+    for d in (Z2C, C2Z):
+        o = oracle.build_route(cu, T, 2, d)
+        thd.swap(x, _gpu_route(cu, T, 2, d), out=out)
+        assert np.array_equal(out.cpu().numpy(), x_np[o.src_of_dst])
+
+
 def test_tiny_workload_payloads():
     """x bf16 [24, 2, 4] and int32 ids, z->c and back, bit for bit."""
     w = W.BY_NAME["tiny"]
