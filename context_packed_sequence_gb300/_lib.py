@@ -25,6 +25,8 @@ ERR_CUDA = 8
 ERR_INDEX_RANGE = 9
 ERR_VALID_EXCEEDS_PADDED = 10
 ERR_CAPACITY = 11
+ERR_SCRATCH_LIMIT = 12
+PACK_NOALLOC_MAX_ROWS = 4096
 
 STATUS_NAMES = {
     OK: "ok",
@@ -39,6 +41,7 @@ STATUS_NAMES = {
     ERR_INDEX_RANGE: "index_range",
     ERR_VALID_EXCEEDS_PADDED: "valid_exceeds_padded",
     ERR_CAPACITY: "capacity",
+    ERR_SCRATCH_LIMIT: "scratch_limit",
 }
 
 ZIGZAG_TO_CONTIGUOUS = 0
@@ -82,6 +85,9 @@ SIGNATURES = {
     "thd_pack_docs": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_int32, c_int32, c_int32, c_int32,
                                 c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
                                 c_size_t, c_void_p, c_void_p]),
+    "thd_pack_docs_noalloc": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_int32, c_int32, c_int32, c_int32,
+                                        c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
+                                        c_void_p]),
     "thd_status_clear": (c_int32, [c_void_p, c_void_p]),
     "thd_status_read": (c_int32, [c_void_p, POINTER(c_int32), c_void_p]),
     "thd_status_string": (c_char_p, [c_int32]),

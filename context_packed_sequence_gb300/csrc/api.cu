@@ -205,6 +205,7 @@ const char* thd_status_string(int32_t code) {
     case THD_ERR_INDEX_RANGE: return "route index out of range";
     case THD_ERR_VALID_EXCEEDS_PADDED: return "unpadded sequence length exceeds padded length";
     case THD_ERR_CAPACITY: return "output capacity exceeded";
+    case THD_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }

@@ -62,7 +62,8 @@ typedef enum thd_status {
   THD_ERR_CUDA = 8,                  /* host: a CUDA call failed, see thd_last_cuda_error() */
   THD_ERR_INDEX_RANGE = 9,           /* device: a route index was outside its buffer */
   THD_ERR_VALID_EXCEEDS_PADDED = 10, /* device: an unpadded length exceeds its padded length */
-  THD_ERR_CAPACITY = 11              /* device: pack_docs output larger than the given capacity */
+  THD_ERR_CAPACITY = 11,             /* device: pack_docs output larger than the given capacity */
+  THD_ERR_SCRATCH_LIMIT = 12         /* host: request larger than thd_pack_docs_noalloc's fixed scratch */
 } thd_status_t;
 
 typedef enum thd_dir {
@@ -234,6 +235,40 @@ thd_status_t thd_pack_docs(const int32_t *raw, int32_t B, int64_t S, int32_t eod
                            int32_t *cu_seqlens, int32_t *cu_seqlens_padded,
                            int64_t docs_capacity, int64_t *counts, void *workspace,
                            size_t workspace_bytes, int32_t *d_status, cudaStream_t stream);
+
+/*
+ * thd_pack_docs without a workspace argument, for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is a
+ * convenience of this library.
+ *
+ * Who needs it: callers that are handed only their input and output buffers,
+ * e.g. a data-loading plugin whose host framework owns all other device
+ * memory through its own pool, or code that must not call cudaMalloc or
+ * cudaFree because those calls can synchronise the device and stall work
+ * queued on other streams.  The call itself allocates nothing and calls no
+ * allocating routine.
+ *
+ * Arguments, results and errors are those of thd_pack_docs, minus the
+ * workspace.  The workspace is a fixed array compiled into the library
+ * (THD_PACK_NOALLOC_MAX_ROWS rows x 32 bytes = 128 KiB), held by every GPU
+ * that loads the library until the process exits:
+ *  - B > THD_PACK_NOALLOC_MAX_ROWS returns THD_ERR_SCRATCH_LIMIT at once and
+ *    enqueues nothing (use thd_pack_docs with your own workspace then);
+ *  - the first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture;
+ *  - all calls on a device share the one array, so calls that may overlap on
+ *    the GPU (different streams, no ordering between them) race and must be
+ *    serialised by the caller.  Calls in order on one stream are safe: each
+ *    call rewrites every scratch entry it reads.
+ */
+#define THD_PACK_NOALLOC_MAX_ROWS 4096
+thd_status_t thd_pack_docs_noalloc(const int32_t *raw, int32_t B, int64_t S, int32_t eod_id,
+                                   int32_t trim_raw_pad, int32_t raw_pad_id, int32_t align,
+                                   int32_t pad_id, int32_t *tokens_out, int64_t tokens_capacity,
+                                   int32_t *cu_seqlens, int32_t *cu_seqlens_padded,
+                                   int64_t docs_capacity, int64_t *counts, int32_t *d_status,
+                                   cudaStream_t stream);
 
 /* Status word helpers.  thd_status_clear enqueues a zero write.
  * thd_status_read copies the word to *host_code and synchronises `stream`:
