@@ -165,6 +165,25 @@ def route_build(cu_seqlens_padded: torch.Tensor, T: int, cp: int, direction: int
     return route
 
 
+def route_build_pair(cu_seqlens_padded: torch.Tensor, T: int, cp: int, status=None,
+                     routes: tuple | None = None, stream=None):
+    """Build both directions' routes in one launch; returns (z2c, c2z)."""
+    _need_cuda(cu_seqlens_padded, "cu_seqlens_padded", torch.int32)
+    if routes is None:
+        dev = cu_seqlens_padded.device
+        routes = (Route(T, cp, ZIGZAG_TO_CONTIGUOUS, dev), Route(T, cp, CONTIGUOUS_TO_ZIGZAG, dev))
+    if status is None:
+        status = new_status(cu_seqlens_padded.device)
+    fwd, bwd = routes
+    fwd.status = bwd.status = status
+    with _range("thd_route_build_pair"):
+        code = L.load().thd_route_build_pair(_ptr(cu_seqlens_padded), cu_seqlens_padded.numel() - 1, int(T),
+                                             int(cp), ctypes.byref(fwd.c), ctypes.byref(bwd.c), _ptr(status),
+                                             _stream(stream))
+    _raise_host(code, "thd_route_build_pair")
+    return fwd, bwd
+
+
 def partition_indices(cu_seqlens_padded: torch.Tensor, T: int, cp: int, rank: int = -1, status=None,
                       out=None, stream=None) -> torch.Tensor:
     """Zigzag slice index of one rank ([T/cp]) or of all ranks ([cp, T/cp])."""
@@ -311,8 +330,13 @@ class RouteCache:
         """Fill both directions at once; nothing to do for cp == 1."""
         if cp == 1:
             return
-        for d in (ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG):
-            self.get(cu, T, cp, d, status=status, stream=stream)
+        key = self._key(cu, T, cp)
+        if all((h := self._slots.get(d)) is not None and h[0] == key and h[1] is cu
+               for d in (ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG)):
+            return
+        fwd, bwd = route_build_pair(cu, T, cp, status=status, stream=stream)
+        self._slots[ZIGZAG_TO_CONTIGUOUS] = (key, cu, fwd)
+        self._slots[CONTIGUOUS_TO_ZIGZAG] = (key, cu, bwd)
 
     def clear(self):
         self._slots.clear()

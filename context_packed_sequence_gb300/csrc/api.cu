@@ -103,8 +103,24 @@ thd_status_t thd_route_build(const int32_t* cu_seqlens_padded, int32_t num_docs,
       num_docs > kMaxRows - 1 || !route_ok(route))
     return THD_ERR_INVALID_ARG;
   if (route->total_rows != T || route->cp_size != cp_size || route->dir != dir) return THD_ERR_INVALID_ARG;
-  return launch_route_build(cu_seqlens_padded, num_docs, static_cast<int32_t>(T), cp_size, dir, route,
-                            d_status, stream);
+  const bool z2c = dir == THD_ZIGZAG_TO_CONTIGUOUS;
+  return launch_route_build(cu_seqlens_padded, num_docs, static_cast<int32_t>(T), cp_size, z2c ? 1 : 2,
+                            z2c ? route : nullptr, z2c ? nullptr : route, d_status, stream);
+}
+
+thd_status_t thd_route_build_pair(const int32_t* cu_seqlens_padded, int32_t num_docs, int64_t T, int32_t cp_size,
+                                  const thd_route_t* route_z2c, const thd_route_t* route_c2z, int32_t* d_status,
+                                  cudaStream_t stream) {
+  if (!route_args_ok(T, cp_size) || !cu_seqlens_padded || !d_status || num_docs < 0 ||
+      num_docs > kMaxRows - 1 || !route_ok(route_z2c) || !route_ok(route_c2z))
+    return THD_ERR_INVALID_ARG;
+  if (route_z2c->dir != THD_ZIGZAG_TO_CONTIGUOUS || route_c2z->dir != THD_CONTIGUOUS_TO_ZIGZAG)
+    return THD_ERR_BAD_DIRECTION;
+  if (route_z2c->total_rows != T || route_c2z->total_rows != T || route_z2c->cp_size != cp_size ||
+      route_c2z->cp_size != cp_size)
+    return THD_ERR_INVALID_ARG;
+  return launch_route_build(cu_seqlens_padded, num_docs, static_cast<int32_t>(T), cp_size, 3, route_z2c,
+                            route_c2z, d_status, stream);
 }
 
 thd_status_t thd_partition_indices(const int32_t* cu_seqlens_padded, int32_t num_docs, int64_t T,

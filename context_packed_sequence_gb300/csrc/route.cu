@@ -3,12 +3,19 @@
 // "[Task32] feat: fla mcore chunkwise cp stage 3" (Relax PR #273), section 2.1:
 // both layouts are unions of global row intervals, so the all-to-all route
 // follows from interval intersection.  The pages copy cu_seqlens to the host
-// and intersect with a Python two-pointer loop; here every block validates
-// the boundaries itself, derives the per-(rank, rank) intersection sizes from
-// a closed-form count of zigzag rows below a position, and then writes each
-// route entry from its own index with a binary search of the boundaries (a
-// gather, so all stores are coalesced).  No host synchronisation, no atomics
-// on the route, one launch per direction.
+// and intersect with a Python two-pointer loop.  Here one kernel per call:
+//
+//  1. every block stages the boundaries in shared memory, validates them
+//     (all blocks reach the same verdict; block 0 writes the status word) and
+//     derives the cp x (cp+1) table "zigzag rows of rank s below d*S" in
+//     closed form, plus the receive offsets;
+//  2. warps walk the zigzag buffer in tiles of 32 consecutive positions
+//     (rank r, slot j).  A tile's documents come from one full search of the
+//     boundaries plus a short window search per lane; the global row g, the
+//     contiguous rank of g and the entry's place in every route array then
+//     follow in closed form, with divisions by S done by multiply-shift.
+//
+// No host synchronisation, no atomics on the route, deterministic.
 #include "thd_internal.cuh"
 
 namespace thd {
@@ -19,19 +26,25 @@ constexpr int kSmemBudget = 48 * 1024;
 
 struct RouteArgs {
   const int32_t* cu;
-  int32_t n, T, cp, S;
+  int32_t n, T, S;
+  CpMath m;
+  FastDiv divS;
   bool cu_in_smem;
-  thd_route_t r;
+  thd_route_t zc;  // zigzag -> contiguous (used when bit 0 of DIRS is set)
+  thd_route_t cz;  // contiguous -> zigzag (used when bit 1 of DIRS is set)
   int32_t* status;
 };
 
-// Does rank-interval [lo, lo+S) of the contiguous layout contain two
+constexpr int kZC = 1, kCZ = 2;
+
+// Does rank-interval [lo, hi) of the contiguous layout contain two
 // neighbouring rows whose zigzag owners decrease?  Owners along a document
 // run 0,1,..,cp-1,cp-1,..,1,0 chunk by chunk, so a decrease happens exactly
 // at the starts of chunks cp+1 .. 2cp-1.  No decrease <=> sorting the
 // interval's rows by (owner, row) keeps them in row order <=> the receive
 // rows of z->c (equally the send rows of c->z) of that rank are 0..S-1.
-__device__ bool has_descent(const int32_t* cu, int32_t n, int32_t cp, int32_t lo, int32_t hi) {
+__device__ bool has_descent(const int32_t* cu, int32_t n, CpMath m, int32_t lo, int32_t hi) {
+  const int32_t cp = m.cp;
   if (cp == 1 || hi <= lo) return false;
   int32_t ilo = doc_of(cu, n, lo), ihi = doc_of(cu, n, hi - 1);
   if (ihi > ilo && cu[ihi] > cu[ilo + 1]) return true;  // a whole non-empty document inside
@@ -40,45 +53,109 @@ __device__ bool has_descent(const int32_t* cu, int32_t n, int32_t cp, int32_t lo
     if (pass == 1 && ihi == ilo) break;
     int32_t L = cu[i + 1] - cu[i];
     if (L == 0) continue;
-    int32_t c = L / (2 * cp);
-    // descents at b = cu[i] + m*c, m = cp+1 .. 2cp-1; need lo+1 <= b <= hi-1
+    int32_t c = m.div2(L);
+    // descents at b = cu[i] + k*c, k = cp+1 .. 2cp-1; need lo+1 <= b <= hi-1
     int32_t a = lo + 1 - cu[i];
-    int32_t mlo = a <= 0 ? cp + 1 : max(cp + 1, (a + c - 1) / c);
+    int32_t klo = a <= 0 ? cp + 1 : max(cp + 1, (a + c - 1) / c);
     int32_t b = hi - 1 - cu[i];
     if (b < 0) continue;
-    int32_t mhi = min(2 * cp - 1, b / c);
-    if (mlo <= mhi) return true;
+    int32_t khi = min(2 * cp - 1, b / c);
+    if (klo <= khi) return true;
   }
   return false;
 }
 
-// Receive row j of contiguous rank d under z->c (the same list is the send
-// row list of contiguous rank d under c->z): the sender s is the rank whose
-// block [roff[d][s], roff[d][s+1]) holds j; the row is the (j - roff[d][s])-th
-// zigzag row of s inside d's interval.
-__device__ __forceinline__ int32_t contiguous_side_row(const int32_t* cu, int32_t n, int32_t cp,
-                                                       int32_t S, const int32_t* cnt,
-                                                       const int32_t* roff, int32_t d, int32_t j) {
-  const int32_t* ro = roff + d * (cp + 1);
-  int32_t s = 0, len = cp;  // largest s in [0, cp) with ro[s] <= j
-  while (len > 1) {
-    int32_t half = len >> 1;
-    s = (ro[s + half] <= j) ? s + half : s;
-    len -= half;
+// Split sizes, offsets and identity flags of one direction (block 0 only).
+// n_zc[s][d] = cnt[s][d+1] - cnt[s][d] rows go from zigzag rank s to
+// contiguous rank d; the reverse direction transposes it.
+__device__ void write_small_arrays(const thd_route_t& r, bool z2c, const int32_t* cu, int32_t n, CpMath m,
+                                   int32_t S, const int32_t* cnt, const int32_t* roff) {
+  const int32_t cp = m.cp;
+  for (int32_t e = threadIdx.x; e < cp * cp; e += blockDim.x) {
+    int32_t x = e / cp, y = e - x * cp;
+    int32_t nxy = cnt[x * (cp + 1) + y + 1] - cnt[x * (cp + 1) + y];  // n_zc[x][y]
+    int32_t nyx = cnt[y * (cp + 1) + x + 1] - cnt[y * (cp + 1) + x];  // n_zc[y][x]
+    r.input_split_sizes[e] = z2c ? nxy : nyx;   // [s=x][d=y]
+    r.output_split_sizes[e] = z2c ? nyx : nxy;  // [d=x][s=y]
   }
-  int32_t slot = cnt[s * (cp + 1) + d] + (j - ro[s]);
-  return zigzag_row(cu, n, cp, s, slot) - d * S;
+  for (int32_t e = threadIdx.x; e < cp * (cp + 1); e += blockDim.x) {
+    r.send_offsets[e] = z2c ? cnt[e] : roff[e];
+    r.recv_offsets[e] = z2c ? roff[e] : cnt[e];
+  }
+  for (int32_t k = threadIdx.x; k < cp; k += blockDim.x) {
+    uint8_t in_order = has_descent(cu, n, m, k * S, (k + 1) * S) ? 0 : 1;
+    r.send_identity[k] = z2c ? 1 : in_order;
+    r.recv_identity[k] = z2c ? in_order : 1;
+  }
 }
 
-template <int DIR>
+// A warp walks a contiguous range of zigzag positions u = r*S + j, 32 per
+// step, and keeps the document index of its lowest slot.  Within one rank
+// the slots only grow, so the next tile's documents are found by galloping
+// forward from there; a full search happens only at the start and where the
+// walk enters another rank.
+struct TileWalker {
+  int32_t doc;      // document of the lowest slot of the previous tile
+  int32_t rank;     // its rank (-1 before the first tile)
+};
+
+struct TileRow {
+  int32_t u, r, j, g;
+};
+
+// Lanes hold positions u (clamped to last, the walk's final position, for
+// the slot arithmetic; such lanes must not store).
+__device__ __forceinline__ TileRow tile_row(const int32_t* cu, int32_t n, CpMath m, int32_t S, FastDiv divS,
+                                            int32_t u, int32_t last, TileWalker& w) {
+  TileRow t;
+  t.u = u;
+  const int32_t uc = min(u, last);
+  t.r = divS.div(uc);
+  t.j = uc - t.r * S;
+  const int32_t r_first = __shfl_sync(kFullMask, t.r, 0), r_last = __shfl_sync(kFullMask, t.r, 31);
+  const int32_t x_lo = __shfl_sync(kFullMask, t.j, 0) * m.cp;
+  const int32_t x_hi = __shfl_sync(kFullMask, t.j, 31) * m.cp;
+  const int32_t x = t.j * m.cp;
+  int32_t i;
+  if (r_first == r_last) {
+    const int32_t i_lo = (w.rank == r_first) ? doc_from(cu, n, w.doc, x_lo) : doc_of(cu, n, x_lo);
+    const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
+    i = doc_in(cu, i_lo, i_hi, x);
+    w.doc = i_lo;
+    w.rank = r_first;
+  } else {  // the tile crosses into the next rank
+    i = doc_of(cu, n, x);
+    w.rank = -1;
+  }
+  const int32_t c0 = cu[i];
+  const int32_t c = m.div2(cu[i + 1] - c0);
+  const int32_t loc = t.j - m.div(c0);
+  t.g = loc < c ? c0 + t.r * c + loc : c0 + (2 * m.cp - 1 - t.r) * c + (loc - c);
+  return t;
+}
+
+// The warp's range of positions [begin, end) out of [0, total): equal shares,
+// whole tiles of 32.
+__device__ __forceinline__ void warp_range(int64_t total, int64_t* begin, int64_t* end) {
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t tiles = (total + 31) / 32;
+  const int64_t per = (tiles + nwarps - 1) / nwarps;
+  *begin = min(total, warp * per * 32);
+  *end = min(total, (warp + 1) * per * 32);
+}
+
+template <int DIRS, bool SMEM_CU>
 __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a) {
   extern __shared__ int32_t smem[];
-  if (block_status_set(a.status)) return;
-  const int32_t cp = a.cp, S = a.S, T = a.T, n = a.n;
+  const CpMath m = a.m;
+  const int32_t cp = m.cp, S = a.S, T = a.T, n = a.n;
   int32_t* cnt = smem;                        // [cp][cp+1]: zigzag rows of s below d*S
   int32_t* roff = cnt + cp * (cp + 1);        // [d][cp+1]: z->c receive offsets
   int32_t* cu_s = roff + cp * (cp + 1);
-  const int32_t* cu = stage_cu(a.cu, n, cu_s, a.cu_in_smem);
+  const int32_t* unused;
+  if (stage_cu_check_status(a.cu, n, cu_s, SMEM_CU, a.status, &unused)) return;
+  const int32_t* cu = SMEM_CU ? cu_s : a.cu;
 
   int32_t code = block_check_cu(cu, n, T, 2 * cp, true);
   if (code != THD_OK) {
@@ -88,7 +165,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
 
   for (int32_t e = threadIdx.x; e < cp * (cp + 1); e += blockDim.x) {
     int32_t s = e / (cp + 1), d = e - s * (cp + 1);
-    cnt[e] = zigzag_count_below(cu, n, cp, S, T, s, d * S);
+    cnt[e] = zigzag_count_below(cu, n, m, S, T, s, d * S);
   }
   __syncthreads();
   for (int32_t d = threadIdx.x; d < cp; d += blockDim.x) {
@@ -101,77 +178,67 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   }
   __syncthreads();
 
-  const thd_route_t& r = a.r;
   if (blockIdx.x == 0) {
-    for (int32_t e = threadIdx.x; e < cp * cp; e += blockDim.x) {
-      int32_t x = e / cp, y = e - x * cp;
-      // n_zc[s][d] = rows zigzag rank s sends to contiguous rank d
-      if (DIR == THD_ZIGZAG_TO_CONTIGUOUS) {
-        int32_t nxy = cnt[x * (cp + 1) + y + 1] - cnt[x * (cp + 1) + y];  // n_zc[x][y]
-        r.input_split_sizes[e] = nxy;   // [s=x][d=y]
-        int32_t nyx = cnt[y * (cp + 1) + x + 1] - cnt[y * (cp + 1) + x];  // n_zc[y][x]
-        r.output_split_sizes[e] = nyx;  // [d=x][s=y]
-      } else {
-        int32_t nyx = cnt[y * (cp + 1) + x + 1] - cnt[y * (cp + 1) + x];  // n_zc[y][x]
-        r.input_split_sizes[e] = nyx;   // [s=x][d=y] = n_zc[d][s]
-        int32_t nxy = cnt[x * (cp + 1) + y + 1] - cnt[x * (cp + 1) + y];  // n_zc[x][y]
-        r.output_split_sizes[e] = nxy;  // [d=x][s=y] = n_zc[d][s]
-      }
-    }
-    for (int32_t e = threadIdx.x; e < cp * (cp + 1); e += blockDim.x) {
-      if (DIR == THD_ZIGZAG_TO_CONTIGUOUS) {
-        r.send_offsets[e] = cnt[e];   // [s][d] = zigzag rows of s below d*S
-        r.recv_offsets[e] = roff[e];  // [d][s]
-      } else {
-        r.send_offsets[e] = roff[e];  // [s][d]
-        r.recv_offsets[e] = cnt[e];   // [d][s]
-      }
-    }
-    for (int32_t k = threadIdx.x; k < cp; k += blockDim.x) {
-      uint8_t reorder = has_descent(cu, n, cp, k * S, (k + 1) * S) ? 0 : 1;
-      if (DIR == THD_ZIGZAG_TO_CONTIGUOUS) {
-        r.send_identity[k] = 1;
-        r.recv_identity[k] = reorder;
-      } else {
-        r.send_identity[k] = reorder;
-        r.recv_identity[k] = 1;
-      }
-    }
+    if (DIRS & kZC) write_small_arrays(a.zc, true, cu, n, m, S, cnt, roff);
+    if (DIRS & kCZ) write_small_arrays(a.cz, false, cu, n, m, S, cnt, roff);
   }
 
-  const int32_t stride = gridDim.x * blockDim.x;
-  for (int32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < T; u += stride) {
-    int32_t rank = u / S;
-    int32_t j = u - rank * S;
-    if (DIR == THD_ZIGZAG_TO_CONTIGUOUS) {
-      r.src_of_dst[u] = zigzag_pos(cu, n, cp, S, u);
-      r.send_rows[u] = j;
-      r.recv_rows[u] = contiguous_side_row(cu, n, cp, S, cnt, roff, rank, j);
-    } else {
-      r.src_of_dst[u] = zigzag_row(cu, n, cp, rank, j);
-      r.send_rows[u] = contiguous_side_row(cu, n, cp, S, cnt, roff, rank, j);
-      r.recv_rows[u] = j;
+  // Zigzag position u = r*S + j holds global row g.  Then
+  //   z->c: src_of_dst[g] = u, send_rows[u] = j;
+  //   c->z: src_of_dst[u] = g, recv_rows[u] = j;
+  //   with d = g / S the contiguous rank of g, the row is entry
+  //   roff[d][r] + (j - cnt[r][d]) of d's z->c receive buffer and of d's c->z
+  //   send buffer, with value g - d*S.
+  int64_t begin, end;
+  warp_range(T, &begin, &end);
+  const FastDiv divS = a.divS;
+  const int32_t lane = threadIdx.x & 31;
+  TileWalker w{0, -1};
+  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
+    const TileRow t = tile_row(cu, n, m, S, divS, static_cast<int32_t>(tile0) + lane,
+                               static_cast<int32_t>(end) - 1, w);
+    if (t.u < end) {
+      const int32_t d = divS.div(t.g);
+      const int32_t pos = d * S + roff[d * (cp + 1) + t.r] + (t.j - cnt[t.r * (cp + 1) + d]);
+      if (DIRS & kZC) {
+        a.zc.src_of_dst[t.g] = t.u;
+        a.zc.send_rows[t.u] = t.j;
+        a.zc.recv_rows[pos] = t.g - d * S;
+      }
+      if (DIRS & kCZ) {
+        a.cz.src_of_dst[t.u] = t.g;
+        a.cz.recv_rows[t.u] = t.j;
+        a.cz.send_rows[pos] = t.g - d * S;
+      }
     }
   }
 }
 
+template <bool SMEM_CU>
 __global__ void __launch_bounds__(kRouteThreads)
-partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, int32_t cp, int32_t S, int32_t rank,
-                 bool cu_in_smem, int32_t* out, int32_t* status) {
+partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, CpMath m, FastDiv divS, int32_t S, int32_t rank,
+                 int32_t* out, int32_t* status) {
   extern __shared__ int32_t smem[];
-  if (block_status_set(status)) return;
-  const int32_t* cu = stage_cu(cu_g, n, smem, cu_in_smem);
-  int32_t code = block_check_cu(cu, n, T, 2 * cp, true);
+  const int32_t* unused;
+  if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
+  const int32_t* cu = SMEM_CU ? smem : cu_g;
+  int32_t code = block_check_cu(cu, n, T, 2 * m.cp, true);
   if (code != THD_OK) {
     if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
     return;
   }
+  // all ranks: out[u] for zigzag positions u in [0, T); one rank r: out[j]
+  // for positions r*S + j, j in [0, S)
   const int32_t total = rank < 0 ? T : S;
-  const int32_t stride = gridDim.x * blockDim.x;
-  for (int32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += stride) {
-    int32_t r = rank < 0 ? u / S : rank;
-    int32_t slot = rank < 0 ? u - r * S : u;
-    out[u] = zigzag_row(cu, n, cp, r, slot);
+  const int32_t base = rank < 0 ? 0 : rank * S;
+  int64_t begin, end;
+  warp_range(total, &begin, &end);
+  const int32_t lane = threadIdx.x & 31;
+  TileWalker w{0, -1};
+  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
+    const int32_t k = static_cast<int32_t>(tile0) + lane;
+    const TileRow t = tile_row(cu, n, m, S, divS, base + k, base + static_cast<int32_t>(end) - 1, w);
+    if (k < end) out[k] = t.g;
   }
 }
 
@@ -185,25 +252,39 @@ int grid_for(int64_t work, int threads, int per_sm) {
 
 }  // namespace
 
-thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t cp, int32_t dir,
-                                const thd_route_t* route, int32_t* status, cudaStream_t s) {
+thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t cp, int32_t dirs,
+                                const thd_route_t* zc, const thd_route_t* cz, int32_t* status,
+                                cudaStream_t s) {
   RouteArgs a;
   a.cu = cu;
   a.n = n;
   a.T = T;
-  a.cp = cp;
   a.S = T / cp;
-  a.r = *route;
+  a.m = make_cp_math(cp);
+  a.divS = make_fast_div(a.S > 0 ? a.S : 1);
+  a.zc = zc ? *zc : thd_route_t{};
+  a.cz = cz ? *cz : thd_route_t{};
   a.status = status;
   size_t tables = static_cast<size_t>(2) * cp * (cp + 1) * sizeof(int32_t);
   size_t cu_bytes = static_cast<size_t>(n + 1) * sizeof(int32_t);
   a.cu_in_smem = tables + cu_bytes <= static_cast<size_t>(kSmemBudget);
   size_t smem = tables + (a.cu_in_smem ? cu_bytes : 0);
   int grid = grid_for(T, kRouteThreads, 2);
-  if (dir == THD_ZIGZAG_TO_CONTIGUOUS)
-    route_build_kernel<THD_ZIGZAG_TO_CONTIGUOUS><<<grid, kRouteThreads, smem, s>>>(a);
-  else
-    route_build_kernel<THD_CONTIGUOUS_TO_ZIGZAG><<<grid, kRouteThreads, smem, s>>>(a);
+  if (a.cu_in_smem) {
+    if (dirs == (kZC | kCZ))
+      route_build_kernel<kZC | kCZ, true><<<grid, kRouteThreads, smem, s>>>(a);
+    else if (dirs == kZC)
+      route_build_kernel<kZC, true><<<grid, kRouteThreads, smem, s>>>(a);
+    else
+      route_build_kernel<kCZ, true><<<grid, kRouteThreads, smem, s>>>(a);
+  } else {
+    if (dirs == (kZC | kCZ))
+      route_build_kernel<kZC | kCZ, false><<<grid, kRouteThreads, smem, s>>>(a);
+    else if (dirs == kZC)
+      route_build_kernel<kZC, false><<<grid, kRouteThreads, smem, s>>>(a);
+    else
+      route_build_kernel<kCZ, false><<<grid, kRouteThreads, smem, s>>>(a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
@@ -218,8 +299,12 @@ thd_status_t launch_partition(const int32_t* cu, int32_t n, int32_t T, int32_t c
   bool in_smem = cu_bytes <= static_cast<size_t>(kSmemBudget);
   int32_t S = T / cp;
   int grid = grid_for(rank < 0 ? T : S, kRouteThreads, 2);
-  partition_kernel<<<grid, kRouteThreads, in_smem ? cu_bytes : 0, s>>>(cu, n, T, cp, S, rank, in_smem,
-                                                                      out, status);
+  const CpMath m = make_cp_math(cp);
+  const FastDiv divS = make_fast_div(S > 0 ? S : 1);
+  if (in_smem)
+    partition_kernel<true><<<grid, kRouteThreads, cu_bytes, s>>>(cu, n, T, m, divS, S, rank, out, status);
+  else
+    partition_kernel<false><<<grid, kRouteThreads, 0, s>>>(cu, n, T, m, divS, S, rank, out, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);

@@ -57,10 +57,12 @@ __device__ __forceinline__ int32_t doc_of(const int32_t* cu, int32_t n, int32_t 
 __device__ __forceinline__ int32_t block_check_cu(const int32_t* cu, int32_t n, int64_t T, int32_t mult,
                                                   bool check_total) {
   int mono_bad = 0, div_bad = 0;
+  // a power-of-two multiple is tested with a mask (the usual 2*cp)
+  const bool pow2 = mult > 0 && (mult & (mult - 1)) == 0;
   for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
     int32_t a = cu[i], b = cu[i + 1];
     if (b < a) mono_bad = 1;
-    else if (mult > 0 && ((b - a) % mult) != 0) div_bad = 1;
+    else if (mult > 0 && (pow2 ? ((b - a) & (mult - 1)) : ((b - a) % mult)) != 0) div_bad = 1;
   }
   int any_mono = __syncthreads_or(mono_bad);
   int any_div = __syncthreads_or(div_bad);
@@ -69,6 +71,35 @@ __device__ __forceinline__ int32_t block_check_cu(const int32_t* cu, int32_t n, 
   if (any_div) return THD_ERR_LEN_NOT_DIVISIBLE;
   if (check_total && static_cast<int64_t>(cu[n]) != T) return THD_ERR_TOTAL_MISMATCH;
   return THD_OK;
+}
+
+// Read the status word (one thread) while the block copies the n+1
+// boundaries into shared memory (when they fit), under one barrier.  Returns
+// true when the status word was already set; *view is the array to search.
+__device__ __forceinline__ bool stage_cu_check_status(const int32_t* cu, int32_t n, int32_t* smem,
+                                                      bool to_smem, const int32_t* st,
+                                                      const int32_t** view) {
+  __shared__ int32_t flag;
+  if (threadIdx.x == 0) flag = status_load(st);
+  if (to_smem) {
+    // four independent loads in flight per thread before the stores
+    for (int32_t base = threadIdx.x; base <= n; base += 4 * blockDim.x) {
+      int32_t v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int32_t i = base + k * static_cast<int32_t>(blockDim.x);
+        v[k] = i <= n ? cu[i] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int32_t i = base + k * static_cast<int32_t>(blockDim.x);
+        if (i <= n) smem[i] = v[k];
+      }
+    }
+  }
+  __syncthreads();
+  *view = to_smem ? smem : cu;
+  return flag != 0;
 }
 
 // Copy n+1 boundaries into shared memory (when they fit) and return the view
@@ -84,45 +115,123 @@ __device__ __forceinline__ const int32_t* stage_cu(const int32_t* cu, int32_t n,
 // zigzag geometry ("Packed Sequence 与上下文并行", section 2.4)
 // ---------------------------------------------------------------------------
 
+// Division by cp and by 2*cp: a shift when cp is a power of two (the usual
+// case), a division otherwise.  Operands are never negative.
+struct CpMath {
+  int32_t cp;
+  int32_t shift;  // log2(cp) when cp is a power of two, else -1
+  __device__ __forceinline__ int32_t div(int32_t x) const { return shift >= 0 ? x >> shift : x / cp; }
+  __device__ __forceinline__ int32_t div2(int32_t x) const {
+    return shift >= 0 ? x >> (shift + 1) : x / (2 * cp);
+  }
+};
+
+inline CpMath make_cp_math(int32_t cp) {
+  CpMath m;
+  m.cp = cp;
+  m.shift = -1;
+  for (int b = 0; b < 31; ++b)
+    if ((1 << b) == cp) m.shift = b;
+  return m;
+}
+
+// floor(n / d) for 0 <= n < 2^31 and 1 <= d < 2^31 by one 64-bit multiply and
+// a shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, theorem 4.2 with N = 31): l = ceil(log2 d),
+// m = ceil(2^(31+l) / d) < 2^33, q = (n * m) >> (31 + l).
+struct FastDiv {
+  uint64_t m;
+  int32_t shift;
+  __device__ __forceinline__ int32_t div(int32_t n) const {
+    return static_cast<int32_t>((static_cast<uint64_t>(n) * m) >> shift);
+  }
+};
+
+inline FastDiv make_fast_div(int32_t d) {
+  FastDiv f;
+  int l = 0;
+  while ((int64_t(1) << l) < d) ++l;
+  f.shift = 31 + l;
+  f.m = ((uint64_t(1) << f.shift) + static_cast<uint64_t>(d) - 1) / static_cast<uint64_t>(d);
+  return f;
+}
+
+// Largest i in [lo, hi] with cu[i] <= x, given cu[lo] <= x.  The length is
+// the same for all lanes of a warp when lo and hi are, so the loop is too.
+__device__ __forceinline__ int32_t doc_in(const int32_t* cu, int32_t lo, int32_t hi, int32_t x) {
+  int32_t len = hi - lo + 1;
+  while (len > 1) {
+    const int32_t half = len >> 1;
+    lo = (cu[lo + half] <= x) ? lo + half : lo;
+    len -= half;
+  }
+  return lo;
+}
+
+// Largest k >= i with cu[k] <= x, given cu[i] <= x: gallop forward from i
+// (1, 2, 4, ... documents), then search the last bracket.  Costs O(log of the
+// distance), so following a position that only moves forward is cheap.
+__device__ __forceinline__ int32_t doc_from(const int32_t* cu, int32_t n, int32_t i, int32_t x) {
+  int32_t step = 1;
+  while (i + step <= n && cu[i + step] <= x) {
+    i += step;
+    step <<= 1;
+  }
+  return doc_in(cu, i, min(i + step - 1, n), x);
+}
+
+// The documents of a warp's 32 consecutive positions: one full search for
+// the lowest and the highest position (lanes 0 and 1 search, everyone gets
+// both answers), then a window search per lane, usually 0-2 steps.  lo_x and
+// hi_x must be the same in every lane, and every lane's x in [lo_x, hi_x].
+__device__ __forceinline__ int32_t warp_doc_of(const int32_t* cu, int32_t n, int32_t lo_x, int32_t hi_x,
+                                               int32_t x) {
+  const int lane = threadIdx.x & 31;
+  const int32_t found = doc_of(cu, n, lane == 0 ? lo_x : hi_x);
+  const int32_t i_lo = __shfl_sync(kFullMask, found, 0);
+  const int32_t i_hi = __shfl_sync(kFullMask, found, 1);
+  return doc_in(cu, i_lo, i_hi, x);
+}
+
 // Global row held by rank r at zigzag slot `slot`.  Rank-local document i
 // starts at slot cu[i]/cp (every padded length is a multiple of 2*cp), so the
 // document is found by searching cu for slot*cp.
-__device__ __forceinline__ int32_t zigzag_row(const int32_t* cu, int32_t n, int32_t cp, int32_t r,
+__device__ __forceinline__ int32_t zigzag_row(const int32_t* cu, int32_t n, CpMath m, int32_t r,
                                               int32_t slot) {
-  int32_t i = doc_of(cu, n, slot * cp);
+  int32_t i = doc_of(cu, n, slot * m.cp);
   int32_t c0 = cu[i];
-  int32_t c = (cu[i + 1] - c0) / (2 * cp);
-  int32_t loc = slot - c0 / cp;
-  return loc < c ? c0 + r * c + loc : c0 + (2 * cp - 1 - r) * c + (loc - c);
+  int32_t c = m.div2(cu[i + 1] - c0);
+  int32_t loc = slot - m.div(c0);
+  return loc < c ? c0 + r * c + loc : c0 + (2 * m.cp - 1 - r) * c + (loc - c);
 }
 
 // Zigzag buffer position (r*S + slot) of global row g.
-__device__ __forceinline__ int32_t zigzag_pos(const int32_t* cu, int32_t n, int32_t cp, int32_t S,
+__device__ __forceinline__ int32_t zigzag_pos(const int32_t* cu, int32_t n, CpMath m, int32_t S,
                                               int32_t g) {
   int32_t i = doc_of(cu, n, g);
   int32_t c0 = cu[i];
-  int32_t c = (cu[i + 1] - c0) / (2 * cp);
+  int32_t c = m.div2(cu[i + 1] - c0);
   int32_t off = g - c0;
   int32_t k = off / c;
   int32_t j = off - k * c;
-  int32_t r = k < cp ? k : 2 * cp - 1 - k;
-  return r * S + c0 / cp + (k < cp ? j : c + j);
+  int32_t r = k < m.cp ? k : 2 * m.cp - 1 - k;
+  return r * S + m.div(c0) + (k < m.cp ? j : c + j);
 }
 
 // Number of zigzag rows of rank r with global index < X (0 <= X <= T):
 // earlier documents give cu[i]/cp rows, document i the clipped overlap of its
 // front chunk [r*c, (r+1)*c) and back chunk [(2cp-1-r)*c, (2cp-r)*c) with
 // [0, X - cu[i]).
-__device__ __forceinline__ int32_t zigzag_count_below(const int32_t* cu, int32_t n, int32_t cp,
+__device__ __forceinline__ int32_t zigzag_count_below(const int32_t* cu, int32_t n, CpMath m,
                                                       int32_t S, int32_t T, int32_t r, int32_t X) {
   if (X >= T) return S;
   int32_t i = doc_of(cu, n, X);
   int32_t c0 = cu[i];
-  int32_t c = (cu[i + 1] - c0) / (2 * cp);
+  int32_t c = m.div2(cu[i + 1] - c0);
   int32_t off = X - c0;
   int32_t a = min(max(off - r * c, 0), c);
-  int32_t b = min(max(off - (2 * cp - 1 - r) * c, 0), c);
-  return c0 / cp + a + b;
+  int32_t b = min(max(off - (2 * m.cp - 1 - r) * c, 0), c);
+  return m.div(c0) + a + b;
 }
 
 // ---------------------------------------------------------------------------
@@ -176,8 +285,10 @@ void record_cuda_error(cudaError_t e);
 int sm_count();
 
 // launchers (one per translation unit); return THD_OK or THD_ERR_CUDA
-thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t cp, int32_t dir,
-                                const thd_route_t* route, int32_t* status, cudaStream_t s);
+// dirs: bit 0 = zigzag->contiguous into zc, bit 1 = contiguous->zigzag into cz
+thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t cp, int32_t dirs,
+                                const thd_route_t* zc, const thd_route_t* cz, int32_t* status,
+                                cudaStream_t s);
 thd_status_t launch_partition(const int32_t* cu, int32_t n, int32_t T, int32_t cp, int32_t rank,
                               int32_t* out, int32_t* status, cudaStream_t s);
 enum CopyKind { COPY_SWAP = 0, COPY_PACK = 1, COPY_A2A = 2, COPY_SCATTER = 3 };

@@ -145,6 +145,21 @@ thd_status_t thd_route_build(const int32_t *cu_seqlens_padded, int32_t num_docs,
                              int32_t *d_status, cudaStream_t stream);
 
 /*
+ * Both directions in one launch: route_z2c (bound with THD_ZIGZAG_TO_CONTIGUOUS)
+ * and route_c2z (bound with THD_CONTIGUOUS_TO_ZIGZAG) for the same T and
+ * cp_size, with the same validation and d_status rules as thd_route_build.
+ * The two routes share the interval counts and half of their rows (the c->z
+ * send rows are the z->c receive rows), so one pass writes both -- what the
+ * pages' prebuild of both directions per microbatch does (Relax PR #273,
+ * section 2.4) in one kernel.  A direction mismatch returns
+ * THD_ERR_BAD_DIRECTION.
+ */
+thd_status_t thd_route_build_pair(const int32_t *cu_seqlens_padded, int32_t num_docs, int64_t T,
+                                  int32_t cp_size, const thd_route_t *route_z2c,
+                                  const thd_route_t *route_c2z, int32_t *d_status,
+                                  cudaStream_t stream);
+
+/*
  * Zigzag partition indices ("Packed Sequence 与上下文并行", section 2.4, what
  * its get_slice_index returns): out[k] = global row held in local slot k.
  *  cp_rank >= 0: out is int32[T/cp] for that rank.

@@ -47,6 +47,10 @@ def test_route_status_matches_oracle(cu, T, cp, direction):
     st = thd.new_status()
     r = thd.route_build(cu_t, T, cp, direction, status=st)
     assert L.STATUS_NAMES[thd.status_read(st)] == want
+    # the two-direction build reports the same failure
+    stp = thd.new_status()
+    thd.route_build_pair(cu_t, T, cp, status=stp)
+    assert L.STATUS_NAMES[thd.status_read(stp)] == want
     # the partition kernel reports the same failure
     st2 = thd.new_status()
     thd.partition_indices(cu_t, T, cp, -1, status=st2)
@@ -69,6 +73,14 @@ def test_host_errors_raise_at_once():
     with pytest.raises(thd.ThdError) as e:
         thd.route_build(cu, 6, 2, Z2C)
     assert e.value.kind == "invalid_arg"
+
+
+def test_pair_refuses_swapped_directions():
+    cu = torch.tensor([0, 8], dtype=torch.int32, device="cuda")
+    fwd, bwd = thd.Route(8, 2, Z2C), thd.Route(8, 2, C2Z)
+    with pytest.raises(thd.ThdError) as e:
+        thd.route_build_pair(cu, 8, 2, routes=(bwd, fwd))
+    assert e.value.kind == "bad_direction"
 
 
 def test_label_status_matches_oracle():

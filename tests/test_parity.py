@@ -28,6 +28,24 @@ def _gpu_route(cu, T, cp, direction):
     return r
 
 
+def _gpu_pair(cu, T, cp):
+    st = thd.new_status()
+    f, b = thd.route_build_pair(_cu_tensor(cu), T, cp, status=st)
+    thd.check_status(st, "route_build_pair")
+    return f, b
+
+
+def _assert_both(cu, T, cp):
+    """Each direction alone and both in one launch, against the oracle."""
+    want = [oracle.build_route(cu, T, cp, d) for d in (Z2C, C2Z)]
+    for d in (Z2C, C2Z):
+        _assert_route(_gpu_route(cu, T, cp, d), want[d])
+    f, b = _gpu_pair(cu, T, cp)
+    _assert_route(f, want[Z2C])
+    _assert_route(b, want[C2Z])
+    return want
+
+
 def _flat(list_of_lists):
     out = []
     for x in list_of_lists:
@@ -85,11 +103,9 @@ def test_route_bruteforce_small_packings():
     n = 0
     for cp, lens in _small_packings():
         cu = _bounds(lens)
-        T = cu[-1]
-        for d in (Z2C, C2Z):
-            _assert_route(_gpu_route(cu, T, cp, d), oracle.build_route(cu, T, cp, d))
-            n += 1
-    assert n > 500
+        _assert_both(cu, cu[-1], cp)
+        n += 1
+    assert n > 250
 
 
 MEDIUM = [
@@ -110,8 +126,7 @@ def test_route_medium(seed, cp, n_docs, max_chunk, empty):
     lens = W.random_lengths(seed, n_docs, cp, max_chunk, empty)
     cu = _bounds(lens)
     T = cu[-1]
-    for d in (Z2C, C2Z):
-        _assert_route(_gpu_route(cu, T, cp, d), oracle.build_route(cu, T, cp, d))
+    _assert_both(cu, T, cp)
     st = thd.new_status()
     got = thd.partition_indices(_cu_tensor(cu), T, cp, -1, status=st)
     thd.check_status(st)
@@ -123,20 +138,16 @@ def test_route_boundaries_beyond_shared_memory(cp, n_docs):
     """Enough documents that the boundaries are searched in global memory."""
     lens = W.random_lengths(99 + cp, n_docs, cp, 2, 0.1)
     cu = _bounds(lens)
-    T = cu[-1]
-    for d in (Z2C, C2Z):
-        _assert_route(_gpu_route(cu, T, cp, d), oracle.build_route(cu, T, cp, d))
+    _assert_both(cu, cu[-1], cp)
 
 
 def test_empty_packing_and_cp1():
     for cu in ([0], [0, 0, 0]):
-        for d in (Z2C, C2Z):
-            _assert_route(_gpu_route(cu, 0, 4, d), oracle.build_route(cu, 0, 4, d))
+        _assert_both(cu, 0, 4)
     cu = _bounds([2, 6, 0, 10])
+    _assert_both(cu, 18, 1)
     for d in (Z2C, C2Z):
-        r = _gpu_route(cu, 18, 1, d)
-        _assert_route(r, oracle.build_route(cu, 18, 1, d))
-        assert r.src_of_dst.cpu().tolist() == list(range(18))
+        assert _gpu_route(cu, 18, 1, d).src_of_dst.cpu().tolist() == list(range(18))
 
 
 # --------------------------------------------------------------------------
@@ -265,6 +276,14 @@ def test_movedim_wrapper_and_cache():
     assert cache.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is not r1
     assert cache.get(cu.clone(), T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is not r1
     assert thd.zigzag_contiguous_thd_swap(x, cu, 1, 0, seq_dim=1) is x  # cp == 1: nothing moves
+    pre = thd.RouteCache()
+    pre.prebuild(cu, T, 2)                                              # both directions, one launch
+    f = pre.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS)
+    b = pre.get(cu, T, 2, thd.CONTIGUOUS_TO_ZIGZAG)
+    assert f.src_of_dst.cpu().tolist() == o.src_of_dst
+    pre.prebuild(cu, T, 2)                                              # still fresh: nothing rebuilt
+    assert pre.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is f and pre.get(cu, T, 2, 1) is b
+    assert thd.RouteCache().prebuild(cu, T, 1) is None                  # cp == 1: nothing to build
 
 
 # --------------------------------------------------------------------------
@@ -324,10 +343,12 @@ def test_pack_docs_random_against_oracle():
 def _full_size_swap_check(cu, cp, hidden, seed, sample=4096):
     T = cu[-1]
     x = W.payload_device(seed, T, hidden, "cuda")
+    pair = _gpu_pair(cu, T, cp)
     for d in (Z2C, C2Z):
         o = oracle.build_route(cu, T, cp, d)
         r = _gpu_route(cu, T, cp, d)
         _assert_route(r, o)
+        _assert_route(pair[d], o)
         st = thd.new_status()
         out = thd.swap(x, r, status=st)
         thd.check_status(st)
