@@ -248,7 +248,7 @@ def run_thd(args, rank, world, local):
         pcu_v = torch.empty(cap_docs, dtype=torch.int32, device=device)
         pcu = torch.empty(cap_docs, dtype=torch.int32, device=device)
         counts = torch.zeros(2, dtype=torch.int64, device=device)
-        ws = torch.empty(lib.thd_pack_docs_workspace_bytes(B), dtype=torch.uint8, device=device)
+        ws = torch.empty(lib.thd_pack_docs_workspace_bytes(B, S), dtype=torch.uint8, device=device)
         labels = torch.empty((w.mtp_depth + 1, T), dtype=torch.int32, device=device)
         lmask = torch.empty((w.mtp_depth + 1, T), dtype=torch.uint8, device=device)
         valid = torch.empty((T,), dtype=torch.uint8, device=device)
@@ -346,6 +346,50 @@ def run_thd(args, rank, world, local):
     route_us = {k: round(statistics.median(v), 2) for k, v in rb.items()}
     route_us["method"] = "median of 50, CUDA events with the GPU kept busy ahead of each launch"
 
+    # packing and labels alone (pipeline workload): CUDA events, median of 20
+    prep = None
+    if extra is not None:
+        e = extra
+
+        def pack_call():
+            lib.thd_pack_docs(e["raw"].data_ptr(), e["B"], e["S"], W.EOD_ID, 0, 0, 2 * cp, 0, e["ptok"].data_ptr(),
+                              e["cap_tok"], e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), e["cap_docs"],
+                              e["counts"].data_ptr(), e["ws"].data_ptr(), e["ws"].numel(), status.data_ptr(), sp)
+
+        def labels_call():
+            lib.thd_roll_labels(e["ptok"].data_ptr(), e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), n_docs, T,
+                                w.mtp_depth, 0, e["labels"].data_ptr(), e["lmask"].data_ptr(), e["valid"].data_ptr(),
+                                status.data_ptr(), sp)
+
+        def time_call(fn):
+            ts = []
+            for it in range(30):
+                torch.cuda._sleep(200_000)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize(device)
+                if it >= 10:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            return statistics.median(ts)
+
+        peak_gbs, _ = measured_peak()
+        raw_tokens = e["B"] * e["S"]
+        pack_bytes = 4 * raw_tokens + 4 * T + 8 * (n_docs + 1)            # read raw once, write tokens + bounds
+        lab_bytes = 4 * T + 8 * (n_docs + 1) + (w.mtp_depth + 1) * 5 * T + T  # tokens in; labels, masks, valid out
+        pack_us, lab_us = time_call(pack_call), time_call(labels_call)
+        prep = {
+            "pack_docs": {"us": round(pack_us, 2), "algorithmic_bytes": pack_bytes,
+                          "gbs": round(pack_bytes / pack_us / 1e3, 1),
+                          "frac_of_measured": round(pack_bytes / pack_us / 1e3 / peak_gbs, 4)},
+            "roll_labels": {"us": round(lab_us, 2), "algorithmic_bytes": lab_bytes, "mtp_depth": w.mtp_depth,
+                            "gbs": round(lab_bytes / lab_us / 1e3, 1),
+                            "frac_of_measured": round(lab_bytes / lab_us / 1e3 / peak_gbs, 4)},
+        }
+        if thd.status_read(status) != 0:
+            raise RuntimeError("device status set while timing packing / labels")
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -399,6 +443,8 @@ def run_thd(args, rank, world, local):
     }
     if e2e is not None:
         result["e2e"] = e2e
+    if prep is not None:
+        result["data_prep_kernels"] = prep
     return result, dict(x=x, T=T, cu=cu_d, w=w, row_bytes=row_bytes)
 
 

@@ -283,7 +283,7 @@ def pack_docs(raw, eod_id: int, align: int, pad_id: int = 0, raw_pad_id=None, st
     cu_v = torch.empty(cap_docs, dtype=torch.int32, device=dev)
     cu = torch.empty(cap_docs, dtype=torch.int32, device=dev)
     counts = torch.zeros(2, dtype=torch.int64, device=dev)
-    ws = torch.empty(max(lib.thd_pack_docs_workspace_bytes(B), 8), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(lib.thd_pack_docs_workspace_bytes(B, S), 8), dtype=torch.uint8, device=dev)
     if status is None:
         status = new_status(dev)
     trim = raw_pad_id is not None

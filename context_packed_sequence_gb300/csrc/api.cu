@@ -164,8 +164,8 @@ thd_status_t thd_roll_labels(const int32_t* tokens, const int32_t* cu_seqlens, c
                             fill, labels, loss_mask, valid_mask, d_status, stream);
 }
 
-size_t thd_pack_docs_workspace_bytes(int32_t B) {
-  return B < 0 ? 0 : static_cast<size_t>(B) * 4 * sizeof(int64_t);
+size_t thd_pack_docs_workspace_bytes(int32_t B, int64_t S) {
+  return (B < 0 || S < 0) ? 0 : pack_docs_chunked_workspace(B, S);
 }
 
 thd_status_t thd_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod_id, int32_t trim_raw_pad,
@@ -177,7 +177,7 @@ thd_status_t thd_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod
       docs_capacity < 1 || !cu_seqlens || !cu_seqlens_padded || !counts || !d_status)
     return THD_ERR_INVALID_ARG;
   if (B > 0 && S > 0 && (!raw || !tokens_out)) return THD_ERR_INVALID_ARG;
-  if (B > 0 && (!workspace || workspace_bytes < thd_pack_docs_workspace_bytes(B) ||
+  if (B > 0 && (!workspace || workspace_bytes < thd_pack_docs_workspace_bytes(B, S) ||
                 reinterpret_cast<uintptr_t>(workspace) % 8 != 0))
     return THD_ERR_INVALID_ARG;
   return launch_pack_docs(raw, B, S, eod_id, trim_raw_pad ? 1 : 0, raw_pad_id, align, pad_id, tokens_out,

@@ -7,7 +7,9 @@
 // these with an O(num_docs) Python fix-up loop and a separate MTP roll; here
 // one kernel writes every depth at once: position p of document i takes
 // tokens[p+1+k] at depth k when p+1+k is still before the document's valid
-// end e_i, else `fill` with mask 0.
+// end e_i, else `fill` with mask 0.  Warps walk contiguous position ranges
+// and follow the current document forward, so finding it costs a step or
+// two per 32 positions instead of a full search per position.
 #include "thd_internal.cuh"
 
 namespace thd {
@@ -16,15 +18,17 @@ namespace {
 constexpr int kLabelThreads = 512;
 constexpr int kSmemBudget = 48 * 1024;
 
+template <bool SMEM_CU>
 __global__ void __launch_bounds__(kLabelThreads)
 roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
-                   int32_t n, int32_t T, int32_t depth, int32_t fill, bool in_smem,
-                   int32_t* __restrict__ labels, uint8_t* __restrict__ lmask,
-                   uint8_t* __restrict__ valid, int32_t* status) {
+                   int32_t n, int32_t T, int32_t depth, int32_t fill, int32_t* __restrict__ labels,
+                   uint8_t* __restrict__ lmask, uint8_t* __restrict__ valid, int32_t* status) {
   extern __shared__ int32_t smem[];
-  if (block_status_set(status)) return;
-  const int32_t* cu = stage_cu(cu_g, n, smem, in_smem);
-  const int32_t* cu_v = stage_cu(cu_v_g, n, smem + (n + 1), in_smem);
+  const int32_t* unused;
+  if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
+  stage_cu(cu_v_g, n, smem + (n + 1), SMEM_CU);
+  const int32_t* cu = SMEM_CU ? smem : cu_g;
+  const int32_t* cu_v = SMEM_CU ? smem + (n + 1) : cu_v_g;
 
   int32_t code = block_check_cu(cu, n, T, 0, true);
   if (code == THD_OK) {
@@ -40,17 +44,36 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
     if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
     return;
   }
+  if (T == 0) return;
 
-  const int32_t stride = gridDim.x * blockDim.x;
-  for (int32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < T; p += stride) {
-    int32_t i = doc_of(cu, n, p);
-    int32_t e = cu[i] + (cu_v[i + 1] - cu_v[i]);
-    valid[p] = p < e ? 1 : 0;
-    for (int32_t k = 0; k <= depth; ++k) {
-      int32_t t = p + 1 + k;
-      bool ok = t < e;
-      labels[static_cast<int64_t>(k) * T + p] = ok ? __ldg(tokens + t) : fill;
-      lmask[static_cast<int64_t>(k) * T + p] = ok ? 1 : 0;
+  // Each warp walks an equal contiguous range of positions, 32 per step,
+  // following the document of its lowest position forward (galloping search).
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t tiles = (static_cast<int64_t>(T) + 31) / 32;
+  const int64_t per = (tiles + nwarps - 1) / nwarps;
+  const int64_t begin = min(static_cast<int64_t>(T), warp * per * 32);
+  const int64_t end = min(static_cast<int64_t>(T), (warp + 1) * per * 32);
+  const int32_t lane = threadIdx.x & 31;
+  int32_t doc = -1;
+  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
+    const int32_t p = static_cast<int32_t>(tile0) + lane;
+    const int32_t pc = min(p, static_cast<int32_t>(end) - 1);
+    const int32_t x_lo = static_cast<int32_t>(tile0);
+    const int32_t x_hi = __shfl_sync(kFullMask, pc, 31);
+    const int32_t i_lo = doc < 0 ? doc_of(cu, n, x_lo) : doc_from(cu, n, doc, x_lo);
+    const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
+    const int32_t i = doc_in(cu, i_lo, i_hi, pc);
+    doc = i_lo;
+    if (p < end) {
+      const int32_t e = cu[i] + (cu_v[i + 1] - cu_v[i]);  // end of the document's valid tokens
+      valid[p] = p < e ? 1 : 0;
+      for (int32_t k = 0; k <= depth; ++k) {
+        const int32_t t = p + 1 + k;
+        const bool ok = t < e;
+        labels[static_cast<int64_t>(k) * T + p] = ok ? __ldg(tokens + t) : fill;
+        lmask[static_cast<int64_t>(k) * T + p] = ok ? 1 : 0;
+      }
     }
   }
 }
@@ -66,8 +89,12 @@ thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, cons
   int64_t cap = static_cast<int64_t>(sm_count()) * 2;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  roll_labels_kernel<<<static_cast<unsigned>(grid), kLabelThreads, in_smem ? bytes : 0, s>>>(
-      tokens, cu_v, cu, n, T, depth, fill, in_smem, labels, lmask, valid, status);
+  if (in_smem)
+    roll_labels_kernel<true><<<static_cast<unsigned>(grid), kLabelThreads, bytes, s>>>(
+        tokens, cu_v, cu, n, T, depth, fill, labels, lmask, valid, status);
+  else
+    roll_labels_kernel<false><<<static_cast<unsigned>(grid), kLabelThreads, 0, s>>>(
+        tokens, cu_v, cu, n, T, depth, fill, labels, lmask, valid, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);

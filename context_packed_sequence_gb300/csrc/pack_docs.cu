@@ -4,15 +4,23 @@
 // every document to the alignment, flatten with document i starting at
 // cu_seqlens_padded[i]) and the worked example of section 3.  The pages do it
 // with bincount/cumsum and a per-document copy loop on the host side of the
-// framework; here two kernels, one block per raw row:
+// framework.  Two device implementations:
 //
-//  1. stats: the row's valid end, its document count and its padded length
-//     (a block-wide max-scan of document ends gives each document's start);
-//  2. emit: every block derives its row's output offset from the stats of the
-//     rows before it, rescans its row and writes tokens, padding and both
-//     boundary arrays.
-//
-// The only scratch is 4 int64 per row between the two kernels.
+//  * chunked (thd_pack_docs): rows are cut into chunks of 2048 tokens, one
+//    block each, so all SMs take part.
+//      0. (only when trimming trailing pads) one block per row finds the
+//         row's valid end;
+//      1. stats: per chunk, its document ends (EODs, and the row's last valid
+//         token), its first and last end, and the padded lengths of the
+//         documents that both start and end inside it;
+//      2. emit: every block scans the statistics of all chunks (a max-scan
+//         carries each row's last end into the next chunk, which fixes the
+//         length of the document open at a chunk boundary; sum-scans give
+//         each chunk's first document index and output offset), then writes
+//         its tokens, padding and boundaries.
+//    Scratch: one int64 per row and four per chunk.
+//  * per row (thd_pack_docs_noalloc, whose scratch is a fixed array of four
+//    int64 per row): the same two phases with one block per raw row.
 #include "thd_internal.cuh"
 
 namespace thd {
@@ -182,9 +190,191 @@ pack_emit_kernel(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t 
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// chunked packing
+// ---------------------------------------------------------------------------
+
+constexpr int kChunkThreads = 256;
+constexpr int kChunkItems = 8;
+constexpr int64_t kChunk = static_cast<int64_t>(kChunkThreads) * kChunkItems;  // tokens per chunk
+
+struct OpMin {
+  template <typename V>
+  __device__ __forceinline__ V operator()(V a, V b) const { return a < b ? a : b; }
+};
+
+struct ChunkGeom {
+  int32_t B;
+  int64_t S;
+  int64_t per_row;  // chunks per row
+  int64_t nc;       // B * per_row
+};
+
+__global__ void __launch_bounds__(kPackThreads)
+pack_row_ends_kernel(const int32_t* raw, int64_t S, int32_t raw_pad, int64_t* ve, int32_t* status) {
+  __shared__ int64_t tmp[32];
+  if (block_status_set(status)) return;
+  const int64_t b = blockIdx.x;
+  const int64_t v = row_valid_end(raw + b * S, S, 1, raw_pad, tmp);
+  if (threadIdx.x == 0) ve[b] = v;
+}
+
+// stats[z] = {ends, first end (-1: none), last end (-1: none), padded length of
+// the documents after the first end}, z = b * per_row + c
+__global__ void __launch_bounds__(kChunkThreads)
+pack_chunk_stats_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64_t* ve_arr, int32_t align,
+                        int64_t* stats, int32_t* status) {
+  __shared__ int64_t tmp[32];
+  if (block_status_set(status)) return;
+  const int64_t b = blockIdx.y, c = blockIdx.x;
+  const int32_t* row = raw + b * g.S;
+  const int64_t ve = ve_arr ? ve_arr[b] : g.S;
+  const int64_t lo = c * kChunk, hi = min(lo + kChunk, ve);
+  const int64_t t0 = lo + static_cast<int64_t>(threadIdx.x) * kChunkItems;
+  int64_t my_first = INT64_MAX, my_last = -1;
+  for (int it = 0; it < kChunkItems; ++it) {
+    const int64_t t = t0 + it;
+    if (t < hi && is_end(row, t, ve, eod)) {
+      if (my_first == INT64_MAX) my_first = t;
+      my_last = t;
+    }
+  }
+  int64_t chunk_last, chunk_first;
+  const int64_t prev = block_exclusive_scan(my_last, OpMax(), static_cast<int64_t>(-1), tmp, &chunk_last);
+  block_exclusive_scan(my_first, OpMin(), INT64_MAX, tmp, &chunk_first);
+  int64_t cnt = 0, psum = 0, pe = prev;
+  for (int it = 0; it < kChunkItems; ++it) {
+    const int64_t t = t0 + it;
+    if (t < hi && is_end(row, t, ve, eod)) {
+      if (pe >= 0) psum += (t - pe) + pad_of(t - pe, align);  // starts inside this chunk
+      ++cnt;
+      pe = t;
+    }
+  }
+  cnt = block_sum(cnt, tmp);
+  psum = block_sum(psum, tmp);
+  if (threadIdx.x == 0) {
+    int64_t* st = stats + (b * g.per_row + c) * 4;
+    st[0] = cnt;
+    st[1] = cnt > 0 ? chunk_first : -1;
+    st[2] = chunk_last;
+    st[3] = psum;
+  }
+}
+
+__global__ void __launch_bounds__(kChunkThreads)
+pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64_t* ve_arr, int32_t align,
+                       int32_t pad_id, const int64_t* stats, int32_t* tokens, int64_t tok_cap, int32_t* cu_v,
+                       int32_t* cu, int64_t docs_cap, int64_t* counts, int32_t* status) {
+  __shared__ int64_t tmp[32];
+  __shared__ int64_t carry[4];  // last end before this chunk in its row, first doc index, output offset
+  if (block_status_set(status)) return;
+  const int64_t b = blockIdx.y, c = blockIdx.x, me = b * g.per_row + c;
+  const int64_t key_span = g.S + 2;  // key = row * key_span + (last end + 1)
+
+  // valid tokens of the rows before this one (the global unpadded offset)
+  int64_t v_before = 0;
+  for (int64_t r = threadIdx.x; r < b; r += blockDim.x) v_before += ve_arr ? ve_arr[r] : g.S;
+  v_before = block_sum(v_before, tmp);
+
+  // every chunk's documents and padded length, in order, 256 chunks a pass
+  int64_t key_carry = -1, docs_carry = 0, pad_carry = 0;
+  for (int64_t base = 0; base < g.nc; base += blockDim.x) {
+    const int64_t z = base + threadIdx.x;
+    int64_t n_end = 0, first = -1, last = -1, tail = 0, key = -1;
+    if (z < g.nc) {
+      const int64_t* st = stats + z * 4;
+      n_end = st[0];
+      first = st[1];
+      last = st[2];
+      tail = st[3];
+      key = (z / g.per_row) * key_span + (last + 1);
+    }
+    int64_t pass_key;
+    int64_t pk = block_exclusive_scan(key, OpMax(), static_cast<int64_t>(-1), tmp, &pass_key);
+    pk = max(pk, key_carry);
+    const int64_t zrow = z / g.per_row;
+    const int64_t prev_end = (pk >= 0 && pk / key_span == zrow) ? pk % key_span - 1 : -1;
+    int64_t pad_len = tail;
+    if (n_end > 0) pad_len += (first - prev_end) + pad_of(first - prev_end, align);
+    int64_t pass_docs, pass_pad;
+    const int64_t docs_before = block_exclusive_scan(n_end, OpSum(), static_cast<int64_t>(0), tmp, &pass_docs);
+    const int64_t pad_before = block_exclusive_scan(pad_len, OpSum(), static_cast<int64_t>(0), tmp, &pass_pad);
+    if (z == me) {
+      carry[0] = prev_end;
+      carry[1] = docs_carry + docs_before;
+      carry[2] = pad_carry + pad_before;
+    }
+    key_carry = max(key_carry, pass_key);
+    docs_carry += pass_docs;
+    pad_carry += pass_pad;
+  }
+  __syncthreads();
+  const int64_t d_all = docs_carry, t_all = pad_carry;
+  const bool over = d_all + 1 > docs_cap || t_all > tok_cap || t_all > INT32_MAX;
+  if (me == 0 && threadIdx.x == 0) {
+    counts[0] = d_all;
+    counts[1] = t_all;
+    if (over) {
+      status_set(status, THD_ERR_CAPACITY);
+    } else {
+      cu[0] = 0;
+      cu_v[0] = 0;
+    }
+  }
+  if (over) return;
+
+  const int32_t* row = raw + b * g.S;
+  const int64_t ve = ve_arr ? ve_arr[b] : g.S;
+  const int64_t lo = c * kChunk, hi = min(lo + kChunk, ve);
+  const int64_t t0 = lo + static_cast<int64_t>(threadIdx.x) * kChunkItems;
+  int64_t my_last = -1;
+  for (int it = 0; it < kChunkItems; ++it) {
+    const int64_t t = t0 + it;
+    if (t < hi && is_end(row, t, ve, eod)) my_last = t;
+  }
+  int64_t unused;
+  int64_t first_prev = block_exclusive_scan(my_last, OpMax(), static_cast<int64_t>(-1), tmp, &unused);
+  first_prev = max(first_prev, carry[0]);
+  int64_t cnt = 0, psum = 0;
+  {
+    int64_t pe = first_prev;
+    for (int it = 0; it < kChunkItems; ++it) {
+      const int64_t t = t0 + it;
+      if (t < hi && is_end(row, t, ve, eod)) {
+        psum += (t - pe) + pad_of(t - pe, align);
+        ++cnt;
+        pe = t;
+      }
+    }
+  }
+  const int64_t cnt_before = block_exclusive_scan(cnt, OpSum(), static_cast<int64_t>(0), tmp, &unused);
+  const int64_t psum_before = block_exclusive_scan(psum, OpSum(), static_cast<int64_t>(0), tmp, &unused);
+  int64_t pe = first_prev;
+  int64_t doc = carry[1] + cnt_before;  // document the next token belongs to
+  int64_t out = carry[2] + psum_before; // that document's first output row
+  for (int it = 0; it < kChunkItems; ++it) {
+    const int64_t t = t0 + it;
+    if (t >= hi) break;
+    const int32_t v = row[t];
+    tokens[out + (t - pe - 1)] = v;
+    if (v == eod || t == ve - 1) {
+      const int64_t L = t - pe;
+      const int64_t P = L + pad_of(L, align);
+      for (int64_t zz = L; zz < P; ++zz) tokens[out + zz] = pad_id;
+      cu_v[doc + 1] = static_cast<int32_t>(v_before + t + 1);
+      cu[doc + 1] = static_cast<int32_t>(out + P);
+      ++doc;
+      out += P;
+      pe = t;
+    }
+  }
+}
+
 }  // namespace
 
-thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t trim,
+thd_status_t launch_pack_docs_rows(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t trim,
                               int32_t raw_pad, int32_t align, int32_t pad_id, int32_t* tokens,
                               int64_t tok_cap, int32_t* cu_v, int32_t* cu, int64_t docs_cap,
                               int64_t* counts, int64_t* ws, int32_t* status, cudaStream_t s) {
@@ -206,6 +396,59 @@ thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t 
   }
   pack_emit_kernel<<<B, kPackThreads, 0, s>>>(raw, B, S, eod, align, pad_id, tokens, tok_cap, cu_v, cu,
                                               docs_cap, counts, ws, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  return THD_OK;
+}
+
+}  // namespace thd
+
+namespace thd {
+
+size_t pack_docs_chunked_workspace(int32_t B, int64_t S) {
+  const int64_t per_row = (S + kChunk - 1) / kChunk;
+  return static_cast<size_t>(B) * sizeof(int64_t) + static_cast<size_t>(B) * per_row * 4 * sizeof(int64_t);
+}
+
+thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t trim,
+                              int32_t raw_pad, int32_t align, int32_t pad_id, int32_t* tokens,
+                              int64_t tok_cap, int32_t* cu_v, int32_t* cu, int64_t docs_cap,
+                              int64_t* counts, int64_t* ws, int32_t* status, cudaStream_t s) {
+  cudaError_t e;
+  if (B == 0 || S == 0) {
+    // no tokens: no documents, T = 0
+    if ((e = cudaMemsetAsync(counts, 0, 2 * sizeof(int64_t), s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(cu, 0, sizeof(int32_t), s)) != cudaSuccess ||
+        (e = cudaMemsetAsync(cu_v, 0, sizeof(int32_t), s)) != cudaSuccess) {
+      record_cuda_error(e);
+      return THD_ERR_CUDA;
+    }
+    return THD_OK;
+  }
+  ChunkGeom g;
+  g.B = B;
+  g.S = S;
+  g.per_row = (S + kChunk - 1) / kChunk;
+  g.nc = static_cast<int64_t>(B) * g.per_row;
+  int64_t* ve = trim ? ws : nullptr;
+  int64_t* stats = ws + B;
+  if (trim) {
+    pack_row_ends_kernel<<<B, kPackThreads, 0, s>>>(raw, S, raw_pad, ws, status);
+    if ((e = cudaGetLastError()) != cudaSuccess) {
+      record_cuda_error(e);
+      return THD_ERR_CUDA;
+    }
+  }
+  const dim3 grid(static_cast<unsigned>(g.per_row), static_cast<unsigned>(B));
+  pack_chunk_stats_kernel<<<grid, kChunkThreads, 0, s>>>(raw, g, eod, ve, align, stats, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  pack_chunk_emit_kernel<<<grid, kChunkThreads, 0, s>>>(raw, g, eod, ve, align, pad_id, stats, tokens, tok_cap,
+                                                        cu_v, cu, docs_cap, counts, status);
   if ((e = cudaGetLastError()) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

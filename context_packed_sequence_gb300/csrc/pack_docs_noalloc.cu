@@ -1,15 +1,15 @@
 // thd_pack_docs_noalloc: document packing for callers that cannot allocate
 // device memory.
 //
-// thd_pack_docs needs a small workspace between its two kernels (4 int64 per
-// raw row) and asks the caller for it.  Some callers have no way to provide
+// thd_pack_docs needs a workspace between its kernels and asks the caller
+// for it.  Some callers have no way to provide
 // one: a data-loading plugin, for instance, that its host framework hands only
 // the input and output buffers while the framework's own pool owns every
 // other byte of device memory, or code that must stay away from
 // cudaMalloc/cudaFree because those calls can synchronise the device and
-// stall work queued on other streams.  This entry point runs the same two
-// kernels with the workspace taken from a fixed array compiled into the
-// library instead.
+// stall work queued on other streams.  This entry point packs with the
+// one-block-per-row kernels, whose workspace is small and fixed per row (4
+// int64), taken from an array compiled into the library instead.
 //
 // The array: kNoAllocMaxRows rows x 4 int64 = 128 KiB, a static __device__
 // variable of this translation unit.  Every GPU that loads the library holds
@@ -74,7 +74,7 @@ extern "C" thd_status_t thd_pack_docs_noalloc(const int32_t* raw, int32_t B, int
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
-  return launch_pack_docs(raw, B, S, eod_id, trim_raw_pad ? 1 : 0, raw_pad_id, align, pad_id, tokens_out,
-                          tokens_capacity, cu_seqlens, cu_seqlens_padded, docs_capacity, counts, scratch,
-                          d_status, stream);
+  return launch_pack_docs_rows(raw, B, S, eod_id, trim_raw_pad ? 1 : 0, raw_pad_id, align, pad_id, tokens_out,
+                               tokens_capacity, cu_seqlens, cu_seqlens_padded, docs_capacity, counts, scratch,
+                               d_status, stream);
 }

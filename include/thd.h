@@ -234,8 +234,9 @@ thd_status_t thd_roll_labels(const int32_t *tokens, const int32_t *cu_seqlens,
  *  tokens_out         device int32[tokens_capacity]
  *  cu_seqlens, cu_seqlens_padded   device int32[docs_capacity]
  *  counts             device int64[2]: {num_docs, T} on completion
- *  workspace          device, >= thd_pack_docs_workspace_bytes(B) bytes,
- *                     8-byte aligned; scratch between the two kernels.
+ *  workspace          device, >= thd_pack_docs_workspace_bytes(B, S) bytes,
+ *                     8-byte aligned; scratch between the kernels (one int64
+ *                     per row and four per 2048-token chunk).
  *  d_status           device int32[1], required; THD_ERR_CAPACITY when
  *                     num_docs+1 > docs_capacity or T > tokens_capacity (then
  *                     nothing but counts is written).
@@ -243,7 +244,7 @@ thd_status_t thd_roll_labels(const int32_t *tokens, const int32_t *cu_seqlens,
  * needs them on the host reads `counts` (one synchronisation, at data-prep
  * time).  T <= B*S*align and num_docs <= B*S always hold.
  */
-size_t thd_pack_docs_workspace_bytes(int32_t B);
+size_t thd_pack_docs_workspace_bytes(int32_t B, int64_t S);
 thd_status_t thd_pack_docs(const int32_t *raw, int32_t B, int64_t S, int32_t eod_id,
                            int32_t trim_raw_pad, int32_t raw_pad_id, int32_t align,
                            int32_t pad_id, int32_t *tokens_out, int64_t tokens_capacity,

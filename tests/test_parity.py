@@ -336,6 +336,22 @@ def test_pack_docs_random_against_oracle():
         assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
 
 
+def test_pack_docs_long_rows_with_trailing_pad():
+    """Rows of several 2048-token chunks whose valid region ends inside a later
+    chunk (trailing pads trimmed), documents crossing chunk boundaries."""
+    rng = np.random.default_rng(12)
+    B, S = 4, 9000
+    raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+    raw[rng.random((B, S)) < 0.002] = 7
+    ends = [9000, 2049, 6143, 0]                  # last row all pad
+    for b, e in enumerate(ends):
+        raw[b, e:] = 0
+    raw[1, 2048] = 7                              # an EOD exactly at a chunk start
+    want = oracle.pack_docs(raw.tolist(), 7, 16, pad_id=5, raw_pad_id=0)
+    got = thd.pack_docs(torch.from_numpy(raw).cuda(), 7, 16, pad_id=5, raw_pad_id=0)
+    assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
+
+
 # --------------------------------------------------------------------------
 # the full-size workloads, in the launch configuration the benchmark times
 # --------------------------------------------------------------------------
