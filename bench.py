@@ -378,7 +378,12 @@ def run_thd(args, rank, world, local):
         raw_tokens = e["B"] * e["S"]
         pack_bytes = 4 * raw_tokens + 4 * T + 8 * (n_docs + 1)            # read raw once, write tokens + bounds
         lab_bytes = 4 * T + 8 * (n_docs + 1) + (w.mtp_depth + 1) * 5 * T + T  # tokens in; labels, masks, valid out
-        pack_us, lab_us = time_call(pack_call), time_call(labels_call)
+        def labels_zz_call():
+            lib.thd_roll_labels_zigzag(e["ptok"].data_ptr(), e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), n_docs, T,
+                                       cp, w.mtp_depth, 0, e["labels"].data_ptr(), e["lmask"].data_ptr(),
+                                       e["valid"].data_ptr(), status.data_ptr(), sp)
+
+        pack_us, lab_us, labz_us = time_call(pack_call), time_call(labels_call), time_call(labels_zz_call)
         prep = {
             "pack_docs": {"us": round(pack_us, 2), "algorithmic_bytes": pack_bytes,
                           "gbs": round(pack_bytes / pack_us / 1e3, 1),
@@ -386,6 +391,9 @@ def run_thd(args, rank, world, local):
             "roll_labels": {"us": round(lab_us, 2), "algorithmic_bytes": lab_bytes, "mtp_depth": w.mtp_depth,
                             "gbs": round(lab_bytes / lab_us / 1e3, 1),
                             "frac_of_measured": round(lab_bytes / lab_us / 1e3 / peak_gbs, 4)},
+            "roll_labels_zigzag": {"us": round(labz_us, 2), "algorithmic_bytes": lab_bytes, "cp_size": cp,
+                                   "gbs": round(lab_bytes / labz_us / 1e3, 1),
+                                   "frac_of_measured": round(lab_bytes / labz_us / 1e3 / peak_gbs, 4)},
         }
         if thd.status_read(status) != 0:
             raise RuntimeError("device status set while timing packing / labels")

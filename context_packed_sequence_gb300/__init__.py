@@ -10,7 +10,7 @@ from .api import (  # noqa: F401
     ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG, ThdError, Route, RouteCache,
     new_status, status_clear, status_read, check_status,
     route_build, route_build_pair, partition_indices, swap, pack, a2a_local, scatter,
-    roll_labels, pack_docs, zigzag_contiguous_thd_swap,
+    roll_labels, roll_labels_zigzag, pack_docs, zigzag_contiguous_thd_swap,
 )
 from . import _lib  # noqa: F401
 

@@ -265,6 +265,30 @@ def roll_labels(tokens, cu_seqlens, cu_seqlens_padded, mtp_depth: int = 0, fill:
     return labels, lmask, valid
 
 
+def roll_labels_zigzag(tokens, cu_seqlens, cu_seqlens_padded, cp: int, mtp_depth: int = 0, fill: int = 0,
+                       status=None, stream=None):
+    """roll_labels in the zigzag layout of cp ranks (rank-major [cp, T/cp]
+    along the last dim): the label roll and the partition gather in one pass."""
+    for t, nme in ((tokens, "tokens"), (cu_seqlens, "cu_seqlens"), (cu_seqlens_padded, "cu_seqlens_padded")):
+        _need_cuda(t, nme, torch.int32)
+    if cu_seqlens.numel() != cu_seqlens_padded.numel() or cu_seqlens.numel() < 1:
+        raise ThdError(L.ERR_INVALID_ARG, "roll_labels_zigzag: boundary arrays differ in length")
+    T = tokens.numel()
+    dev = tokens.device
+    labels = torch.empty((mtp_depth + 1, T), dtype=torch.int32, device=dev)
+    lmask = torch.empty((mtp_depth + 1, T), dtype=torch.uint8, device=dev)
+    valid = torch.empty((T,), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    with _range("thd_roll_labels_zigzag"):
+        code = L.load().thd_roll_labels_zigzag(_ptr(tokens), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
+                                               cu_seqlens.numel() - 1, T, int(cp), int(mtp_depth), int(fill),
+                                               _ptr(labels), _ptr(lmask), _ptr(valid), _ptr(status),
+                                               _stream(stream))
+    _raise_host(code, "thd_roll_labels_zigzag")
+    return labels, lmask, valid
+
+
 def pack_docs(raw, eod_id: int, align: int, pad_id: int = 0, raw_pad_id=None, status=None, stream=None,
               tokens_capacity=None):
     """Pack raw [B, S] int32 rows into (tokens [T], cu_seqlens, cu_seqlens_padded).

@@ -164,6 +164,18 @@ thd_status_t thd_roll_labels(const int32_t* tokens, const int32_t* cu_seqlens, c
                             fill, labels, loss_mask, valid_mask, d_status, stream);
 }
 
+thd_status_t thd_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_seqlens,
+                                    const int32_t* cu_seqlens_padded, int32_t num_docs, int64_t T, int32_t cp_size,
+                                    int32_t mtp_depth, int32_t fill, int32_t* labels, uint8_t* loss_mask,
+                                    uint8_t* valid_mask, int32_t* d_status, cudaStream_t stream) {
+  if (!route_args_ok(T, cp_size) || num_docs < 0 || num_docs > kMaxRows - 1 || mtp_depth < 0 || mtp_depth > 64 ||
+      !cu_seqlens || !cu_seqlens_padded || !d_status)
+    return THD_ERR_INVALID_ARG;
+  if (T > 0 && (!tokens || !labels || !loss_mask || !valid_mask)) return THD_ERR_INVALID_ARG;
+  return launch_roll_labels_zigzag(tokens, cu_seqlens, cu_seqlens_padded, num_docs, static_cast<int32_t>(T),
+                                   cp_size, mtp_depth, fill, labels, loss_mask, valid_mask, d_status, stream);
+}
+
 size_t thd_pack_docs_workspace_bytes(int32_t B, int64_t S) {
   return (B < 0 || S < 0) ? 0 : pack_docs_chunked_workspace(B, S);
 }

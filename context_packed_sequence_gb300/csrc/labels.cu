@@ -78,7 +78,84 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
   }
 }
 
+// The same labels written in the zigzag layout: position p = r*S + j of the
+// zigzag buffer holds global row g, so out[k][p] = labels[k][g] (and the same
+// for the masks) -- the label roll and the partition gather in one pass.
+template <bool SMEM_CU>
+__global__ void __launch_bounds__(kLabelThreads)
+roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
+                          int32_t n, int32_t T, CpMath m, FastDiv divS, int32_t depth, int32_t fill,
+                          int32_t* __restrict__ labels, uint8_t* __restrict__ lmask, uint8_t* __restrict__ valid,
+                          int32_t* status) {
+  extern __shared__ int32_t smem[];
+  const int32_t* unused;
+  if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
+  stage_cu(cu_v_g, n, smem + (n + 1), SMEM_CU);
+  const int32_t* cu = SMEM_CU ? smem : cu_g;
+  const int32_t* cu_v = SMEM_CU ? smem + (n + 1) : cu_v_g;
+
+  int32_t code = block_check_cu(cu, n, T, 2 * m.cp, true);
+  if (code == THD_OK) {
+    code = block_check_cu(cu_v, n, 0, 0, false);
+    if (code == THD_OK) {
+      int bad = 0;
+      for (int32_t i = threadIdx.x; i < n; i += blockDim.x)
+        if (cu_v[i + 1] - cu_v[i] > cu[i + 1] - cu[i]) bad = 1;
+      if (__syncthreads_or(bad)) code = THD_ERR_VALID_EXCEEDS_PADDED;
+    }
+  }
+  if (code != THD_OK) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
+    return;
+  }
+  const int32_t S = T / m.cp;
+  int64_t begin, end;
+  warp_range(T, &begin, &end);
+  const int32_t lane = threadIdx.x & 31;
+  TileWalker w{0, -1};
+  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
+    const TileRow t = tile_row(cu, n, m, S, divS, static_cast<int32_t>(tile0) + lane,
+                               static_cast<int32_t>(end) - 1, w);
+    if (t.u < end) {
+      const int32_t e = cu[t.doc] + (cu_v[t.doc + 1] - cu_v[t.doc]);
+      valid[t.u] = t.g < e ? 1 : 0;
+      for (int32_t k = 0; k <= depth; ++k) {
+        const int32_t tt = t.g + 1 + k;
+        const bool ok = tt < e;
+        labels[static_cast<int64_t>(k) * T + t.u] = ok ? __ldg(tokens + tt) : fill;
+        lmask[static_cast<int64_t>(k) * T + t.u] = ok ? 1 : 0;
+      }
+    }
+  }
+}
+
 }  // namespace
+
+thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu, int32_t n,
+                                       int32_t T, int32_t cp, int32_t depth, int32_t fill, int32_t* labels,
+                                       uint8_t* lmask, uint8_t* valid, int32_t* status, cudaStream_t s) {
+  size_t bytes = static_cast<size_t>(2) * (n + 1) * sizeof(int32_t);
+  bool in_smem = bytes <= static_cast<size_t>(kSmemBudget);
+  int64_t grid = (static_cast<int64_t>(T) + kLabelThreads - 1) / kLabelThreads;
+  int64_t cap = static_cast<int64_t>(sm_count()) * 2;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  const int32_t S = T / cp;
+  const CpMath m = make_cp_math(cp);
+  const FastDiv divS = make_fast_div(S > 0 ? S : 1);
+  if (in_smem)
+    roll_labels_zigzag_kernel<true><<<static_cast<unsigned>(grid), kLabelThreads, bytes, s>>>(
+        tokens, cu_v, cu, n, T, m, divS, depth, fill, labels, lmask, valid, status);
+  else
+    roll_labels_zigzag_kernel<false><<<static_cast<unsigned>(grid), kLabelThreads, 0, s>>>(
+        tokens, cu_v, cu, n, T, m, divS, depth, fill, labels, lmask, valid, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  return THD_OK;
+}
 
 thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu,
                                 int32_t n, int32_t T, int32_t depth, int32_t fill, int32_t* labels,

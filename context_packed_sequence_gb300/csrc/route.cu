@@ -89,62 +89,6 @@ __device__ void write_small_arrays(const thd_route_t& r, bool z2c, const int32_t
   }
 }
 
-// A warp walks a contiguous range of zigzag positions u = r*S + j, 32 per
-// step, and keeps the document index of its lowest slot.  Within one rank
-// the slots only grow, so the next tile's documents are found by galloping
-// forward from there; a full search happens only at the start and where the
-// walk enters another rank.
-struct TileWalker {
-  int32_t doc;      // document of the lowest slot of the previous tile
-  int32_t rank;     // its rank (-1 before the first tile)
-};
-
-struct TileRow {
-  int32_t u, r, j, g;
-};
-
-// Lanes hold positions u (clamped to last, the walk's final position, for
-// the slot arithmetic; such lanes must not store).
-__device__ __forceinline__ TileRow tile_row(const int32_t* cu, int32_t n, CpMath m, int32_t S, FastDiv divS,
-                                            int32_t u, int32_t last, TileWalker& w) {
-  TileRow t;
-  t.u = u;
-  const int32_t uc = min(u, last);
-  t.r = divS.div(uc);
-  t.j = uc - t.r * S;
-  const int32_t r_first = __shfl_sync(kFullMask, t.r, 0), r_last = __shfl_sync(kFullMask, t.r, 31);
-  const int32_t x_lo = __shfl_sync(kFullMask, t.j, 0) * m.cp;
-  const int32_t x_hi = __shfl_sync(kFullMask, t.j, 31) * m.cp;
-  const int32_t x = t.j * m.cp;
-  int32_t i;
-  if (r_first == r_last) {
-    const int32_t i_lo = (w.rank == r_first) ? doc_from(cu, n, w.doc, x_lo) : doc_of(cu, n, x_lo);
-    const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
-    i = doc_in(cu, i_lo, i_hi, x);
-    w.doc = i_lo;
-    w.rank = r_first;
-  } else {  // the tile crosses into the next rank
-    i = doc_of(cu, n, x);
-    w.rank = -1;
-  }
-  const int32_t c0 = cu[i];
-  const int32_t c = m.div2(cu[i + 1] - c0);
-  const int32_t loc = t.j - m.div(c0);
-  t.g = loc < c ? c0 + t.r * c + loc : c0 + (2 * m.cp - 1 - t.r) * c + (loc - c);
-  return t;
-}
-
-// The warp's range of positions [begin, end) out of [0, total): equal shares,
-// whole tiles of 32.
-__device__ __forceinline__ void warp_range(int64_t total, int64_t* begin, int64_t* end) {
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t tiles = (total + 31) / 32;
-  const int64_t per = (tiles + nwarps - 1) / nwarps;
-  *begin = min(total, warp * per * 32);
-  *end = min(total, (warp + 1) * per * 32);
-}
-
 template <int DIRS, bool SMEM_CU>
 __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a) {
   extern __shared__ int32_t smem[];

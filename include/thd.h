@@ -222,6 +222,24 @@ thd_status_t thd_roll_labels(const int32_t *tokens, const int32_t *cu_seqlens,
                              cudaStream_t stream);
 
 /*
+ * thd_roll_labels written directly in the zigzag layout of cp_size ranks:
+ * position p = r*S + j of the zigzag buffer (S = T/cp_size) holds global row
+ * g = the partition index of (r, j), and
+ *   labels[k*T + p] = (the thd_roll_labels label of row g at depth k),
+ * likewise loss_mask and valid_mask.  The label roll and the zigzag slicing
+ * that "Packed Sequence 与上下文并行" section 2.4 applies to tokens, labels,
+ * loss mask and valid mask alike, in one pass.  Checks: cp_size and T as for
+ * thd_route_build; then the padded boundaries (start, monotone, lengths
+ * multiples of 2*cp_size, total), the unpadded ones (start, monotone), and
+ * valid lengths <= padded lengths.
+ */
+thd_status_t thd_roll_labels_zigzag(const int32_t *tokens, const int32_t *cu_seqlens,
+                                    const int32_t *cu_seqlens_padded, int32_t num_docs, int64_t T,
+                                    int32_t cp_size, int32_t mtp_depth, int32_t fill, int32_t *labels,
+                                    uint8_t *loss_mask, uint8_t *valid_mask, int32_t *d_status,
+                                    cudaStream_t stream);
+
+/*
  * Pack raw rows into one padded THD sequence ("Packed Sequence 与上下文并行",
  * section 2.2 and the worked example of section 3).  Row b's valid region is
  * raw[b][0 .. ve_b) where ve_b is one past its last token != raw_pad_id (the

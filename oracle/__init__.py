@@ -9,5 +9,5 @@ from .thd_oracle import (  # noqa: F401
     ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG, ThdValueError, Route,
     validate_route_args, compact_boundaries, zigzag_partition, contiguous_partition,
     partition_indices, build_route, pack, all_to_all, scatter, apply_route,
-    validate_label_args, roll_labels, pack_docs,
+    validate_label_args, roll_labels, roll_labels_zigzag, pack_docs,
 )

@@ -353,6 +353,21 @@ def roll_labels(tokens, cu_v, cu, depth, fill=0):
     return labels, lmask, valid
 
 
+def roll_labels_zigzag(tokens, cu_v, cu, cp, depth, fill=0):
+    """roll_labels, then the zigzag slicing of every output ([PSCP] 2.4 slices
+    tokens, labels, loss mask and valid mask with the same index): position
+    r*S + j holds the values of global row partition_indices(cu, T, cp, r)[j].
+
+    Checks: the route's checks for (cu, T, cp) first, then the label checks."""
+    T = len(tokens)
+    validate_route_args(cu, T, cp, ZIGZAG_TO_CONTIGUOUS)
+    labels, lmask, valid = roll_labels(tokens, cu_v, cu, depth, fill)
+    idx = partition_indices(cu, T, cp, -1)
+    return ([[row[g] for g in idx] for row in labels],
+            [[row[g] for g in idx] for row in lmask],
+            [valid[g] for g in idx])
+
+
 # --------------------------------------------------------------------------
 # pack raw rows into one padded THD sequence ([PSCP] 2.2, 3.2-3.4)
 # --------------------------------------------------------------------------

@@ -99,6 +99,21 @@ def test_label_status_matches_oracle():
         assert L.STATUS_NAMES[thd.status_read(st)] == want, (tokens, cu_v, cu)
 
 
+def test_zigzag_label_status_matches_oracle():
+    cases = [
+        ([1, 2, 3, 4, 5, 6, 7, 8], [0, 3, 8], [0, 4, 8], 2),      # fine
+        ([1, 2, 3, 4, 5, 6, 7, 8], [0, 3, 8], [0, 2, 8], 2),      # padded length 2 not a multiple of 4
+        ([1, 2, 3, 4, 5, 6, 7, 8], [0, 5, 6], [0, 4, 8], 2),      # valid exceeds padded
+        ([1, 2, 3, 4, 5, 6, 7, 8], [0, 3, 2], [0, 4, 8], 2),      # unpadded not monotone
+    ]
+    dev = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    for tokens, cu_v, cu, cp in cases:
+        want = _oracle_kind(oracle.roll_labels_zigzag, tokens, cu_v, cu, cp, 0)
+        st = thd.new_status()
+        thd.roll_labels_zigzag(dev(tokens), dev(cu_v), dev(cu), cp, 0, status=st)
+        assert L.STATUS_NAMES[thd.status_read(st)] == want, (cu_v, cu)
+
+
 def test_status_is_sticky_until_cleared():
     good = torch.tensor([0, 8, 16], dtype=torch.int32, device="cuda")
     bad = torch.tensor([0, 6, 16], dtype=torch.int32, device="cuda")

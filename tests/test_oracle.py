@@ -311,6 +311,24 @@ def test_labels_worked_example():
     assert [UNSYM.get(t, t) for t in labels[0][0:4]] == ["b", "c", "E", -1]
 
 
+def test_labels_in_zigzag_layout_worked_example():
+    """[PSCP] 3.6 prints each rank's valid mask after the CP slice; the labels
+    sliced the same way follow from 3.8 (next token of the same document)."""
+    g = _golden("pscp_worked_example.json")
+    raw = [[SYM[s] for s in row] for row in g["raw"]]
+    tokens, cu_v, cu = oracle.pack_docs(raw, SYM["E"], g["align"], SYM["P"], SYM["_"])
+    labels, lmask, valid = oracle.roll_labels_zigzag(tokens, cu_v, cu, g["cp"], depth=1, fill=-1)
+    assert valid == g["rank_valid_mask"][0] + g["rank_valid_mask"][1]
+    # rank 0 holds rows 0,3,4,7,8,9,14,15 = a E d P f g P P: labels b - e - g h - -
+    assert [UNSYM.get(t, t) for t in labels[0][:8]] == ["b", -1, "e", -1, "g", "h", -1, -1]
+    # depth 1 for rank 1 (rows 1,2,5,6,10,11,12,13 = b c e E h i j E): d E - - j E - -
+    assert [UNSYM.get(t, t) for t in labels[1][8:]] == ["E", -1, -1, -1, "j", "E", -1, -1]
+    assert sum(lmask[0]) == 13 - 3
+    with pytest.raises(O.ThdValueError) as e:
+        oracle.roll_labels_zigzag(tokens, cu_v, [0, 4, 7, 16], 2, 0)
+    assert e.value.kind == "len_not_divisible"
+
+
 @pytest.mark.parametrize("depth", [0, 1, 3])
 def test_labels_never_cross_documents(depth):
     rng = np.random.default_rng(11 + depth)

@@ -310,6 +310,26 @@ def test_roll_labels_parity(depth):
         assert got[2].cpu().tolist() == want[2]
 
 
+@pytest.mark.parametrize("cp,depth", [(1, 0), (2, 1), (4, 3), (8, 2)])
+def test_roll_labels_zigzag_parity(cp, depth):
+    rng = np.random.default_rng(70 + cp)
+    for trial in range(8):
+        n = int(rng.integers(0, 80))
+        lp = [2 * cp * int(rng.integers(0, 12)) for _ in range(n)]
+        lv = [min(L, int(rng.integers(0, L + 3))) if L else 0 for L in lp]
+        cu_v, cu = _bounds(lv), _bounds(lp)
+        T = cu[-1]
+        tokens = [int(t) for t in rng.integers(0, 151936, size=T)]
+        want = oracle.roll_labels_zigzag(tokens, cu_v, cu, cp, depth, fill=-7)
+        st = thd.new_status()
+        got = thd.roll_labels_zigzag(torch.tensor(tokens, dtype=torch.int32, device="cuda"), _cu_tensor(cu_v),
+                                     _cu_tensor(cu), cp, depth, -7, status=st)
+        thd.check_status(st)
+        assert got[0].cpu().tolist() == want[0]
+        assert got[1].cpu().tolist() == want[1]
+        assert got[2].cpu().tolist() == want[2]
+
+
 def test_pack_docs_worked_example_and_corners():
     E = 99
     cases = [
@@ -397,4 +417,8 @@ def test_full_size_pipeline():
     assert labels.cpu().tolist() == lab_o
     assert lmask.cpu().tolist() == msk_o
     assert valid.cpu().tolist() == val_o
+    # the same labels in the zigzag layout of cp=8 ranks
+    zl, zm, zv = thd.roll_labels_zigzag(tok, cu_v, cu, w.cp, w.mtp_depth, fill=0)
+    idx = torch.tensor(oracle.partition_indices(cu_o, len(tok_o), w.cp, -1), device="cuda").long()
+    assert torch.equal(zl, labels[:, idx]) and torch.equal(zm, lmask[:, idx]) and torch.equal(zv, valid[idx])
     _full_size_swap_check(cu_o, w.cp, w.hidden, w.seed, sample=2048)
