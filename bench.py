@@ -398,6 +398,34 @@ def run_thd(args, rank, world, local):
         if thd.status_read(status) != 0:
             raise RuntimeError("device status set while timing packing / labels")
 
+    # Ulysses exchange of the same hidden states (each token row = cp head groups)
+    uly = None
+    if row_bytes % cp == 0 and T % cp == 0:
+        def uly_time(direction, src, dst):
+            ts = []
+            for it in range(25):
+                if it == 0 or it % 5 == 0:
+                    torch.cuda._sleep(200_000)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                lib.thd_ulysses_swap(src.data_ptr(), dst.data_ptr(), T, cp, row_bytes, direction, status.data_ptr(),
+                                     sp)
+                b.record(stream)
+                torch.cuda.synchronize(device)
+                if it >= 5:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            return statistics.median(ts)
+
+        peak_gbs, _ = measured_peak()
+        to_head = uly_time(0, x, y)
+        to_seq = uly_time(1, y, x)
+        if thd.status_read(status) != 0:
+            raise RuntimeError("device status set by the Ulysses exchange")
+        uly = {"piece_bytes": row_bytes // cp, "seq_to_head_us": round(to_head, 2),
+               "head_to_seq_us": round(to_seq, 2),
+               "gbs": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3, 1),
+               "frac_of_measured": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3 / peak_gbs, 4)}
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -453,6 +481,8 @@ def run_thd(args, rank, world, local):
         result["e2e"] = e2e
     if prep is not None:
         result["data_prep_kernels"] = prep
+    if uly is not None:
+        result["ulysses_swap"] = uly
     return result, dict(x=x, T=T, cu=cu_d, w=w, row_bytes=row_bytes)
 
 

@@ -7,9 +7,9 @@ package is its thin torch binding.
 """
 
 from .api import (  # noqa: F401
-    ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG, ThdError, Route, RouteCache,
+    ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG, SEQ_TO_HEAD, HEAD_TO_SEQ, ThdError, Route, RouteCache,
     new_status, status_clear, status_read, check_status,
-    route_build, route_build_pair, partition_indices, swap, pack, a2a_local, scatter,
+    route_build, route_build_pair, partition_indices, swap, pack, a2a_local, scatter, ulysses_swap,
     roll_labels, roll_labels_zigzag, pack_docs, zigzag_contiguous_thd_swap,
 )
 from . import _lib  # noqa: F401

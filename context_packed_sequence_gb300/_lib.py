@@ -46,6 +46,8 @@ STATUS_NAMES = {
 
 ZIGZAG_TO_CONTIGUOUS = 0
 CONTIGUOUS_TO_ZIGZAG = 1
+SEQ_TO_HEAD = 0
+HEAD_TO_SEQ = 1
 MAX_CP = 64
 
 
@@ -81,6 +83,7 @@ SIGNATURES = {
     "thd_pack": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
     "thd_a2a_local": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
     "thd_scatter": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
+    "thd_ulysses_swap": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int32, c_void_p, c_void_p]),
     "thd_roll_labels": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int64, c_int32, c_int32,
                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "thd_roll_labels_zigzag": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int64, c_int32, c_int32, c_int32,

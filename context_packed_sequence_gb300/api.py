@@ -21,6 +21,8 @@ from . import _lib as L
 
 ZIGZAG_TO_CONTIGUOUS = L.ZIGZAG_TO_CONTIGUOUS
 CONTIGUOUS_TO_ZIGZAG = L.CONTIGUOUS_TO_ZIGZAG
+SEQ_TO_HEAD = L.SEQ_TO_HEAD
+HEAD_TO_SEQ = L.HEAD_TO_SEQ
 
 _NVTX = os.environ.get("THD_NVTX", "0") == "1"
 
@@ -237,6 +239,40 @@ def a2a_local(send, route: Route, out=None, status=None, stream=None):
 def scatter(recv, route: Route, out=None, status=None, stream=None):
     """out[d][recv_rows[d][j]] = recv[d][j]."""
     return _copy("thd_scatter", recv, route, out, status, stream)
+
+
+def ulysses_swap(x, cp: int, direction: int, out=None, status=None, stream=None):
+    """Ulysses exchange between sequence shards and head shards.
+
+    SEQ_TO_HEAD: x is [T, H, ...] (rank r's sequence shard = rows
+    [r*T/cp, (r+1)*T/cp)); returns [cp, T, H/cp, ...], rank r holding every
+    token's heads [r*H/cp, (r+1)*H/cp).  HEAD_TO_SEQ: the inverse."""
+    _need_cuda(x, "x")
+    if direction == SEQ_TO_HEAD:
+        if x.dim() < 2 or x.shape[1] % cp:
+            raise ValueError("x must be [T, H, ...] with H a multiple of cp")
+        T = x.shape[0]
+        shape = (cp, T, x.shape[1] // cp) + tuple(x.shape[2:])
+    elif direction == HEAD_TO_SEQ:
+        if x.dim() < 3 or x.shape[0] != cp:
+            raise ValueError("x must be [cp, T, H/cp, ...]")
+        T = x.shape[1]
+        shape = (T, cp * x.shape[2]) + tuple(x.shape[3:])
+    else:
+        raise ThdError(L.ERR_BAD_DIRECTION, "ulysses_swap")
+    if out is None:
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    _need_cuda(out, "out")
+    if tuple(out.shape) != shape or out.dtype != x.dtype:
+        raise ValueError(f"out must be {shape} of {x.dtype}")
+    if x.numel() == 0:
+        return out
+    row_bytes = x.numel() // T * x.element_size()
+    with _range("thd_ulysses_swap"):
+        code = L.load().thd_ulysses_swap(_ptr(x), _ptr(out), T, int(cp), row_bytes, int(direction), _ptr(status),
+                                         _stream(stream))
+    _raise_host(code, "thd_ulysses_swap")
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -153,6 +153,19 @@ thd_status_t thd_scatter(const void* recv_buf, void* dst, int64_t row_bytes, con
   return copy_entry(COPY_SCATTER, recv_buf, dst, row_bytes, route, d_status, stream);
 }
 
+thd_status_t thd_ulysses_swap(const void* src, void* dst, int64_t T, int32_t cp_size, int64_t row_bytes,
+                              thd_ulysses_dir_t dir, int32_t* d_status, cudaStream_t stream) {
+  if (dir != THD_SEQ_TO_HEAD && dir != THD_HEAD_TO_SEQ) return THD_ERR_BAD_DIRECTION;
+  if (cp_size < 1 || cp_size > THD_MAX_CP || T < 0 || T % cp_size != 0 || T * cp_size > kMaxRows ||
+      row_bytes <= 0 || row_bytes > kMaxRowBytes || row_bytes % cp_size != 0)
+    return THD_ERR_INVALID_ARG;
+  const int64_t bytes = T * row_bytes;
+  if (bytes > 0 && (!src || !dst)) return THD_ERR_INVALID_ARG;
+  if (ranges_overlap(src, dst, bytes)) return THD_ERR_INVALID_ARG;
+  return launch_ulysses(src, dst, static_cast<int32_t>(T), cp_size, row_bytes, dir == THD_SEQ_TO_HEAD, d_status,
+                        stream);
+}
+
 thd_status_t thd_roll_labels(const int32_t* tokens, const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
                              int32_t num_docs, int64_t T, int32_t mtp_depth, int32_t fill, int32_t* labels,
                              uint8_t* loss_mask, uint8_t* valid_mask, int32_t* d_status, cudaStream_t stream) {

@@ -96,6 +96,25 @@ struct A2AMap {
   }
 };
 
+// Ulysses head <-> sequence exchange ("Packed Sequence 与上下文并行", sections
+// 2.5 and 2.7): each token row is cp pieces (head groups) of P bytes.  The
+// sequence-sharded buffer is [T][cp] pieces (token-major), the head-sharded
+// one [cp][T] (rank r holds every token's group r).  The linear side is the
+// destination's pieces.
+struct UlyssesMap {
+  int32_t T, cp;
+  bool seq_to_head;
+  FastDiv div;  // by T (seq -> head) or by cp (head -> seq)
+  __device__ __forceinline__ int32_t operator()(int32_t q) const {
+    if (seq_to_head) {  // destination piece (r, g) <- source piece (g, r)
+      const int32_t r = div.div(q), g = q - r * T;
+      return g * cp + r;
+    }
+    const int32_t g = div.div(q), r = q - g * cp;  // destination (g, r) <- source (r, g)
+    return r * T + g;
+  }
+};
+
 // ---- the unit engine -------------------------------------------------------
 
 struct Walk {
@@ -490,6 +509,13 @@ thd_status_t dispatch_unit(const void* src, void* dst, int32_t rows, int64_t row
 }
 
 }  // namespace
+
+thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes, bool seq_to_head,
+                            int32_t* status, cudaStream_t s) {
+  if (T == 0) return THD_OK;
+  const UlyssesMap map{T, cp, seq_to_head, make_fast_div(seq_to_head ? T : cp)};
+  return dispatch_unit<UlyssesMap, false>(src, dst, T * cp, row_bytes / cp, map, status, s);
+}
 
 thd_status_t launch_copy(CopyKind kind, const void* src, void* dst, int64_t row_bytes,
                          const thd_route_t* r, int32_t* status, cudaStream_t s) {

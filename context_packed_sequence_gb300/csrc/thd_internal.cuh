@@ -356,6 +356,8 @@ thd_status_t launch_partition(const int32_t* cu, int32_t n, int32_t T, int32_t c
 enum CopyKind { COPY_SWAP = 0, COPY_PACK = 1, COPY_A2A = 2, COPY_SCATTER = 3 };
 thd_status_t launch_copy(CopyKind kind, const void* src, void* dst, int64_t row_bytes,
                          const thd_route_t* route, int32_t* status, cudaStream_t s);
+thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes, bool seq_to_head,
+                            int32_t* status, cudaStream_t s);
 thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu,
                                 int32_t n, int32_t T, int32_t depth, int32_t fill, int32_t* labels,
                                 uint8_t* lmask, uint8_t* valid, int32_t* status, cudaStream_t s);

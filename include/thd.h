@@ -71,6 +71,11 @@ typedef enum thd_dir {
   THD_CONTIGUOUS_TO_ZIGZAG = 1
 } thd_dir_t;
 
+typedef enum thd_ulysses_dir {
+  THD_SEQ_TO_HEAD = 0,
+  THD_HEAD_TO_SEQ = 1
+} thd_ulysses_dir_t;
+
 /* Largest supported cp_size. */
 #define THD_MAX_CP 64
 
@@ -197,6 +202,26 @@ thd_status_t thd_a2a_local(const void *send_buf, void *recv_buf, int64_t row_byt
                            const thd_route_t *route, int32_t *d_status, cudaStream_t stream);
 thd_status_t thd_scatter(const void *recv_buf, void *dst, int64_t row_bytes,
                          const thd_route_t *route, int32_t *d_status, cudaStream_t stream);
+
+/*
+ * Ulysses sequence <-> head exchange ("Packed Sequence 与上下文并行",
+ * section 2.5: Ulysses slices the packed sequence into cp contiguous
+ * shards; section 2.7: an all-to-all then gives every rank the whole
+ * sequence for a subset of the heads).  Every token row of row_bytes bytes
+ * is cp head groups of row_bytes/cp bytes (group r = heads
+ * [r*H/cp, (r+1)*H/cp) when the row is [H][...]).
+ *   THD_SEQ_TO_HEAD: src = [T][row] (rank r's shard = rows [r*T/cp, (r+1)*T/cp)),
+ *                    dst = [cp][T][row/cp]: dst[r][g] = group r of src row g.
+ *   THD_HEAD_TO_SEQ: the inverse.
+ * With all ranks in one buffer the exchange is a block transpose.
+ *  T          0 <= T, a multiple of cp_size, T*cp_size < 2^31.
+ *  row_bytes  > 0, a multiple of cp_size; pieces of >= 256 bytes that are a
+ *             multiple of 16 (16-byte aligned buffers) move by TMA bulk copies.
+ *  d_status   as for thd_swap.  A bad dir returns THD_ERR_BAD_DIRECTION.
+ */
+thd_status_t thd_ulysses_swap(const void *src, void *dst, int64_t T, int32_t cp_size,
+                              int64_t row_bytes, thd_ulysses_dir_t dir, int32_t *d_status,
+                              cudaStream_t stream);
 
 /*
  * Document-bounded labels, MTP targets and the valid-token mask

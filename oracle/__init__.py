@@ -10,4 +10,5 @@ from .thd_oracle import (  # noqa: F401
     validate_route_args, compact_boundaries, zigzag_partition, contiguous_partition,
     partition_indices, build_route, pack, all_to_all, scatter, apply_route,
     validate_label_args, roll_labels, roll_labels_zigzag, pack_docs,
+    SEQ_TO_HEAD, HEAD_TO_SEQ, ulysses_swap,
 )

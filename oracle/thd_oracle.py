@@ -294,6 +294,50 @@ def apply_route(x, route):
 
 
 # --------------------------------------------------------------------------
+# Ulysses: sequence shards <-> head shards ([PSCP] 2.5, 2.7)
+# --------------------------------------------------------------------------
+
+SEQ_TO_HEAD = 0
+HEAD_TO_SEQ = 1
+
+
+def ulysses_swap(x, cp, direction):
+    """x: [T, row_bytes] uint8 (SEQ_TO_HEAD) or [cp*T, row_bytes/cp] (HEAD_TO_SEQ).
+
+    Ulysses slices the packed sequence into cp contiguous shards ([PSCP] 2.5)
+    and its all-to-all leaves every rank the whole sequence for a subset of
+    the heads ([PSCP] 2.7).  Reading: rank r gets head group r, the r-th of cp
+    equal slices of each token row.  One piece at a time:
+    SEQ_TO_HEAD: out[r*T + g] = x[g][r*P:(r+1)*P];  HEAD_TO_SEQ: the inverse.
+    """
+    import numpy as np  # byte storage only
+
+    if direction not in (SEQ_TO_HEAD, HEAD_TO_SEQ):
+        raise ThdValueError(BAD_DIRECTION, f"invalid Ulysses direction {direction!r}")
+    if cp < 1:
+        raise ThdValueError(INVALID_ARG, f"cp_size must be >= 1, got {cp}")
+    if direction == SEQ_TO_HEAD:
+        T, row = x.shape
+        if T % cp or row % cp:
+            raise ThdValueError(INVALID_ARG, "T and the row must split into cp parts")
+        P = row // cp
+        out = np.zeros((cp * T, P), dtype=x.dtype)
+        for r in range(cp):
+            for g in range(T):
+                out[r * T + g] = x[g, r * P:(r + 1) * P]
+        return out
+    rows, P = x.shape
+    if rows % cp or (rows // cp) % cp:
+        raise ThdValueError(INVALID_ARG, "rows must split into cp ranks of a multiple of cp tokens")
+    T = rows // cp
+    out = np.zeros((T, cp * P), dtype=x.dtype)
+    for r in range(cp):
+        for g in range(T):
+            out[g, r * P:(r + 1) * P] = x[r * T + g]
+    return out
+
+
+# --------------------------------------------------------------------------
 # labels, MTP targets and the valid mask ([PSCP] 1.3, 1.6, 3.8)
 # --------------------------------------------------------------------------
 

@@ -83,6 +83,17 @@ def test_pair_refuses_swapped_directions():
     assert e.value.kind == "bad_direction"
 
 
+def test_ulysses_host_checks():
+    lib = L.load()
+    x = torch.zeros(8, 64, dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(x)
+    s = torch.cuda.current_stream().cuda_stream
+    assert lib.thd_ulysses_swap(x.data_ptr(), y.data_ptr(), 8, 2, 64, 5, None, s) == L.ERR_BAD_DIRECTION
+    assert lib.thd_ulysses_swap(x.data_ptr(), y.data_ptr(), 8, 3, 64, 0, None, s) == L.ERR_INVALID_ARG   # 8 % 3
+    assert lib.thd_ulysses_swap(x.data_ptr(), y.data_ptr(), 8, 2, 63, 0, None, s) == L.ERR_INVALID_ARG   # row % cp
+    assert lib.thd_ulysses_swap(x.data_ptr(), x.data_ptr() + 64, 8, 2, 64, 0, None, s) == L.ERR_INVALID_ARG
+
+
 def test_label_status_matches_oracle():
     cases = [
         ([1, 2, 3, 4], [0, 5], [0, 4]),

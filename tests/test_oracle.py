@@ -414,6 +414,39 @@ def test_pack_docs_invariants():
 
 
 # --------------------------------------------------------------------------
+# Ulysses exchange ([PSCP] 2.5, 2.7)
+# --------------------------------------------------------------------------
+
+def test_ulysses_hand_example_and_invariants():
+    # 4 tokens x 2 heads of one byte, cp=2: token g is [2g, 2g+1]; rank 0 ends up
+    # with every token's head 0, rank 1 with every token's head 1
+    x = np.arange(8, dtype=np.uint8).reshape(4, 2)
+    assert oracle.ulysses_swap(x, 2, O.SEQ_TO_HEAD).tolist() == [[0], [2], [4], [6], [1], [3], [5], [7]]
+    rng = np.random.default_rng(4)
+    for cp, T, H, D in [(1, 6, 3, 2), (2, 8, 4, 3), (4, 12, 8, 1), (3, 9, 6, 5)]:
+        # byte (g, h, d) identifies its token and head
+        x = np.zeros((T, H * D), dtype=np.uint8)
+        for g in range(T):
+            for h in range(H):
+                x[g, h * D:(h + 1) * D] = (g * 17 + h * 5) % 251
+        y = oracle.ulysses_swap(x, cp, O.SEQ_TO_HEAD)
+        Hg = H // cp
+        for r in range(cp):
+            for g in range(T):
+                # rank r holds the whole sequence, heads [r*H/cp, (r+1)*H/cp), in order
+                want = [(g * 17 + h * 5) % 251 for h in range(r * Hg, (r + 1) * Hg) for _ in range(D)]
+                assert y[r * T + g].tolist() == want
+        assert np.array_equal(oracle.ulysses_swap(y, cp, O.HEAD_TO_SEQ), x)
+        if cp == 1:
+            assert np.array_equal(y, x)
+        z = rng.integers(0, 256, size=(T, H * D), dtype=np.uint8)
+        assert np.array_equal(oracle.ulysses_swap(oracle.ulysses_swap(z, cp, 0), cp, 1), z)
+    with pytest.raises(O.ThdValueError) as e:
+        oracle.ulysses_swap(x, 2, 7)
+    assert e.value.kind == "bad_direction"
+
+
+# --------------------------------------------------------------------------
 # mutation tests: a planted slip in the oracle must fail a pin
 # --------------------------------------------------------------------------
 

@@ -227,6 +227,44 @@ def test_unaligned_buffers_take_the_narrow_path():
         assert np.array_equal(out.cpu().numpy(), x_np[o.src_of_dst])
 
 
+@pytest.mark.parametrize("cp,T,heads,head_bytes", [
+    (2, 64, 8, 64),     # 256-byte pieces: bulk engine
+    (4, 96, 8, 64),     # 128-byte pieces: unit engine, 16-byte units
+    (8, 64, 32, 256),   # 1 KiB pieces, as the 128K workloads
+    (2, 30, 2, 6),      # 6-byte pieces: byte units
+    (1, 16, 4, 32),
+])
+def test_ulysses_parity(cp, T, heads, head_bytes):
+    rng = np.random.default_rng(cp * 100 + T)
+    x_np = rng.integers(0, 256, size=(T, heads * head_bytes), dtype=np.uint8)
+    want = oracle.ulysses_swap(x_np, cp, oracle.SEQ_TO_HEAD)
+    x = torch.from_numpy(x_np).cuda().view(T, heads, head_bytes)
+    st = thd.new_status()
+    y = thd.ulysses_swap(x, cp, thd.SEQ_TO_HEAD, status=st)
+    back = thd.ulysses_swap(y, cp, thd.HEAD_TO_SEQ, status=st)
+    thd.check_status(st)
+    assert tuple(y.shape) == (cp, T, heads // cp, head_bytes)
+    assert np.array_equal(y.cpu().numpy().reshape(cp * T, -1), want)
+    assert np.array_equal(back.cpu().numpy().reshape(T, -1), oracle.ulysses_swap(want, cp, oracle.HEAD_TO_SEQ))
+    assert torch.equal(back, x)
+
+
+def test_zigzag_to_ulysses_and_back():
+    """Zigzag shards -> contiguous (= Ulysses sequence shards) -> head shards,
+    then all the way back, on bf16 hidden states [T, 16, 128]."""
+    cu = _bounds(W.random_lengths(77, 30, 4, 20, 0.1))
+    T = cu[-1]
+    x = W.payload_host(5, T, (16, 128)).cuda()
+    fwd, bwd = _gpu_pair(cu, T, 4)
+    heads = thd.ulysses_swap(thd.swap(x, fwd), 4, thd.SEQ_TO_HEAD)
+    seq = thd.ulysses_swap(heads, 4, thd.HEAD_TO_SEQ)
+    assert torch.equal(thd.swap(seq, bwd), x)
+    o = oracle.build_route(cu, T, 4, Z2C)
+    xc = x.cpu()[torch.tensor(o.src_of_dst)]
+    for r in range(4):
+        assert torch.equal(heads[r].cpu(), xc[:, 4 * r:4 * (r + 1)])
+
+
 def test_tiny_workload_payloads():
     """x bf16 [24, 2, 4] and int32 ids, z->c and back, bit for bit."""
     w = W.BY_NAME["tiny"]
