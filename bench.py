@@ -270,11 +270,12 @@ def run_thd(args, rank, world, local):
         """Everything before the swaps: (packing and labels,) partition, routes."""
         if extra is not None:
             e = extra
-            lib.thd_pack_docs(e["raw"].data_ptr(), e["B"], e["S"], W.EOD_ID, 0, 0, 2 * cp, 0, e["ptok"].data_ptr(),
-                              e["cap_tok"], e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), e["cap_docs"],
+            lib.thd_pack_docs(e["raw"].data_ptr(), e["B"], e["S"], W.EOD_ID, 0, 0, 2 * cp, 0, None,
+                              e["ptok"].data_ptr(), e["cap_tok"], e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), None,
+                              None, e["cap_docs"],
                               e["counts"].data_ptr(), e["ws"].data_ptr(), e["ws"].numel(), status.data_ptr(), s)
             lib.thd_roll_labels(e["ptok"].data_ptr(), e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), n_docs, T,
-                                w.mtp_depth, 0, e["labels"].data_ptr(), e["lmask"].data_ptr(),
+                                w.mtp_depth, 0, None, None, e["labels"].data_ptr(), e["lmask"].data_ptr(),
                                 e["valid"].data_ptr(), status.data_ptr(), s)
         lib.thd_partition_indices(cu_d.data_ptr(), n_docs, T, cp, -1, pidx.data_ptr(), status.data_ptr(), s)
         lib.thd_route_build_pair(cu_d.data_ptr(), n_docs, T, cp, ctypes.byref(fwd.c), ctypes.byref(bwd.c),
@@ -352,14 +353,15 @@ def run_thd(args, rank, world, local):
         e = extra
 
         def pack_call():
-            lib.thd_pack_docs(e["raw"].data_ptr(), e["B"], e["S"], W.EOD_ID, 0, 0, 2 * cp, 0, e["ptok"].data_ptr(),
-                              e["cap_tok"], e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), e["cap_docs"],
+            lib.thd_pack_docs(e["raw"].data_ptr(), e["B"], e["S"], W.EOD_ID, 0, 0, 2 * cp, 0, None,
+                              e["ptok"].data_ptr(), e["cap_tok"], e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), None,
+                              None, e["cap_docs"],
                               e["counts"].data_ptr(), e["ws"].data_ptr(), e["ws"].numel(), status.data_ptr(), sp)
 
         def labels_call():
             lib.thd_roll_labels(e["ptok"].data_ptr(), e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), n_docs, T,
-                                w.mtp_depth, 0, e["labels"].data_ptr(), e["lmask"].data_ptr(), e["valid"].data_ptr(),
-                                status.data_ptr(), sp)
+                                w.mtp_depth, 0, None, None, e["labels"].data_ptr(), e["lmask"].data_ptr(),
+                                e["valid"].data_ptr(), status.data_ptr(), sp)
 
         def time_call(fn):
             ts = []
@@ -378,9 +380,10 @@ def run_thd(args, rank, world, local):
         raw_tokens = e["B"] * e["S"]
         pack_bytes = 4 * raw_tokens + 4 * T + 8 * (n_docs + 1)            # read raw once, write tokens + bounds
         lab_bytes = 4 * T + 8 * (n_docs + 1) + (w.mtp_depth + 1) * 5 * T + T  # tokens in; labels, masks, valid out
+
         def labels_zz_call():
             lib.thd_roll_labels_zigzag(e["ptok"].data_ptr(), e["pcu_v"].data_ptr(), e["pcu"].data_ptr(), n_docs, T,
-                                       cp, w.mtp_depth, 0, e["labels"].data_ptr(), e["lmask"].data_ptr(),
+                                       cp, w.mtp_depth, 0, None, None, e["labels"].data_ptr(), e["lmask"].data_ptr(),
                                        e["valid"].data_ptr(), status.data_ptr(), sp)
 
         pack_us, lab_us, labz_us = time_call(pack_call), time_call(labels_call), time_call(labels_zz_call)

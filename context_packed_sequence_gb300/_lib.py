@@ -85,13 +85,13 @@ SIGNATURES = {
     "thd_scatter": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
     "thd_ulysses_swap": (c_int32, [c_void_p, c_void_p, c_int64, c_int32, c_int64, c_int32, c_void_p, c_void_p]),
     "thd_roll_labels": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int64, c_int32, c_int32,
-                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "thd_roll_labels_zigzag": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int64, c_int32, c_int32, c_int32,
-                                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+                                         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "thd_pack_docs_workspace_bytes": (c_size_t, [c_int32, c_int64]),
     "thd_pack_docs": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_int32, c_int32, c_int32, c_int32,
-                                c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
-                                c_size_t, c_void_p, c_void_p]),
+                                c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
+                                c_void_p, c_void_p, c_size_t, c_void_p, c_void_p]),
     "thd_pack_docs_noalloc": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_int32, c_int32, c_int32, c_int32,
                                         c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
                                         c_void_p]),

@@ -279,9 +279,24 @@ def ulysses_swap(x, cp: int, direction: int, out=None, status=None, stream=None)
 # labels and packing
 # ---------------------------------------------------------------------------
 
+def _next_arrays(next_token, has_next, n_docs):
+    if (next_token is None) != (has_next is None):
+        raise ValueError("next_token and has_next go together")
+    if next_token is not None:
+        _need_cuda(next_token, "next_token", torch.int32)
+        _need_cuda(has_next, "has_next", torch.uint8)
+        if next_token.numel() < n_docs or has_next.numel() < n_docs:
+            raise ValueError("next_token / has_next need one entry per document")
+    return _ptr(next_token), _ptr(has_next)
+
+
 def roll_labels(tokens, cu_seqlens, cu_seqlens_padded, mtp_depth: int = 0, fill: int = 0, status=None,
-                stream=None):
-    """(labels [D+1, T] int32, loss_mask [D+1, T] uint8, valid_mask [T] uint8)."""
+                stream=None, next_token=None, has_next=None):
+    """(labels [D+1, T] int32, loss_mask [D+1, T] uint8, valid_mask [T] uint8).
+
+    next_token / has_next (per document, from pack_docs with row_next): a
+    document cut by the end of its sample continues with the sample's extra
+    token, which becomes the target one past its last valid token."""
     for t, n in ((tokens, "tokens"), (cu_seqlens, "cu_seqlens"), (cu_seqlens_padded, "cu_seqlens_padded")):
         _need_cuda(t, n, torch.int32)
     if cu_seqlens.numel() != cu_seqlens_padded.numel() or cu_seqlens.numel() < 1:
@@ -293,16 +308,17 @@ def roll_labels(tokens, cu_seqlens, cu_seqlens_padded, mtp_depth: int = 0, fill:
     valid = torch.empty((T,), dtype=torch.uint8, device=dev)
     if status is None:
         status = new_status(dev)
+    nt, hn = _next_arrays(next_token, has_next, cu_seqlens.numel() - 1)
     with _range("thd_roll_labels"):
         code = L.load().thd_roll_labels(_ptr(tokens), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
-                                        cu_seqlens.numel() - 1, T, int(mtp_depth), int(fill), _ptr(labels),
-                                        _ptr(lmask), _ptr(valid), _ptr(status), _stream(stream))
+                                        cu_seqlens.numel() - 1, T, int(mtp_depth), int(fill), nt, hn,
+                                        _ptr(labels), _ptr(lmask), _ptr(valid), _ptr(status), _stream(stream))
     _raise_host(code, "thd_roll_labels")
     return labels, lmask, valid
 
 
 def roll_labels_zigzag(tokens, cu_seqlens, cu_seqlens_padded, cp: int, mtp_depth: int = 0, fill: int = 0,
-                       status=None, stream=None):
+                       status=None, stream=None, next_token=None, has_next=None):
     """roll_labels in the zigzag layout of cp ranks (rank-major [cp, T/cp]
     along the last dim): the label roll and the partition gather in one pass."""
     for t, nme in ((tokens, "tokens"), (cu_seqlens, "cu_seqlens"), (cu_seqlens_padded, "cu_seqlens_padded")):
@@ -316,19 +332,22 @@ def roll_labels_zigzag(tokens, cu_seqlens, cu_seqlens_padded, cp: int, mtp_depth
     valid = torch.empty((T,), dtype=torch.uint8, device=dev)
     if status is None:
         status = new_status(dev)
+    nt, hn = _next_arrays(next_token, has_next, cu_seqlens.numel() - 1)
     with _range("thd_roll_labels_zigzag"):
         code = L.load().thd_roll_labels_zigzag(_ptr(tokens), _ptr(cu_seqlens), _ptr(cu_seqlens_padded),
                                                cu_seqlens.numel() - 1, T, int(cp), int(mtp_depth), int(fill),
-                                               _ptr(labels), _ptr(lmask), _ptr(valid), _ptr(status),
+                                               nt, hn, _ptr(labels), _ptr(lmask), _ptr(valid), _ptr(status),
                                                _stream(stream))
     _raise_host(code, "thd_roll_labels_zigzag")
     return labels, lmask, valid
 
 
 def pack_docs(raw, eod_id: int, align: int, pad_id: int = 0, raw_pad_id=None, status=None, stream=None,
-              tokens_capacity=None):
+              tokens_capacity=None, row_next=None):
     """Pack raw [B, S] int32 rows into (tokens [T], cu_seqlens, cu_seqlens_padded).
 
+    row_next (int32 [B], optional): each row's extra token; then the result
+    also holds next_token, has_next per document for roll_labels.
     T and the document count are only known on the device; this call reads
     them back once (a synchronisation, at data-preparation time)."""
     _need_cuda(raw, "raw", torch.int32)
@@ -343,16 +362,26 @@ def pack_docs(raw, eod_id: int, align: int, pad_id: int = 0, raw_pad_id=None, st
     cu_v = torch.empty(cap_docs, dtype=torch.int32, device=dev)
     cu = torch.empty(cap_docs, dtype=torch.int32, device=dev)
     counts = torch.zeros(2, dtype=torch.int64, device=dev)
+    next_token = has_next = None
+    if row_next is not None:
+        _need_cuda(row_next, "row_next", torch.int32)
+        if row_next.numel() != B:
+            raise ValueError("row_next needs one token per row")
+        next_token = torch.empty(cap_docs, dtype=torch.int32, device=dev)
+        has_next = torch.empty(cap_docs, dtype=torch.uint8, device=dev)
     ws = torch.empty(max(lib.thd_pack_docs_workspace_bytes(B, S), 8), dtype=torch.uint8, device=dev)
     if status is None:
         status = new_status(dev)
     trim = raw_pad_id is not None
     code = lib.thd_pack_docs(_ptr(raw), B, S, int(eod_id), int(trim), int(raw_pad_id) if trim else 0, int(align),
-                             int(pad_id), _ptr(tokens), cap_tok, _ptr(cu_v), _ptr(cu), cap_docs, _ptr(counts),
-                             _ptr(ws), ws.numel(), _ptr(status), _stream(stream))
+                             int(pad_id), _ptr(row_next), _ptr(tokens), cap_tok, _ptr(cu_v), _ptr(cu),
+                             _ptr(next_token), _ptr(has_next), cap_docs, _ptr(counts), _ptr(ws), ws.numel(),
+                             _ptr(status), _stream(stream))
     _raise_host(code, "thd_pack_docs")
     check_status(status, "thd_pack_docs", stream)
     n, T = (int(v) for v in counts.tolist())
+    if row_next is not None:
+        return tokens[:T], cu_v[:n + 1], cu[:n + 1], next_token[:n], has_next[:n]
     return tokens[:T], cu_v[:n + 1], cu[:n + 1]
 
 

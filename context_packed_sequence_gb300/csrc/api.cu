@@ -167,26 +167,31 @@ thd_status_t thd_ulysses_swap(const void* src, void* dst, int64_t T, int32_t cp_
 }
 
 thd_status_t thd_roll_labels(const int32_t* tokens, const int32_t* cu_seqlens, const int32_t* cu_seqlens_padded,
-                             int32_t num_docs, int64_t T, int32_t mtp_depth, int32_t fill, int32_t* labels,
+                             int32_t num_docs, int64_t T, int32_t mtp_depth, int32_t fill,
+                             const int32_t* next_token, const uint8_t* has_next, int32_t* labels,
                              uint8_t* loss_mask, uint8_t* valid_mask, int32_t* d_status, cudaStream_t stream) {
+  if ((next_token == nullptr) != (has_next == nullptr)) return THD_ERR_INVALID_ARG;
   if (T < 0 || T > kMaxRows || num_docs < 0 || num_docs > kMaxRows - 1 || mtp_depth < 0 || mtp_depth > 64 ||
       !cu_seqlens || !cu_seqlens_padded || !d_status)
     return THD_ERR_INVALID_ARG;
   if (T > 0 && (!tokens || !labels || !loss_mask || !valid_mask)) return THD_ERR_INVALID_ARG;
   return launch_roll_labels(tokens, cu_seqlens, cu_seqlens_padded, num_docs, static_cast<int32_t>(T), mtp_depth,
-                            fill, labels, loss_mask, valid_mask, d_status, stream);
+                            fill, next_token, has_next, labels, loss_mask, valid_mask, d_status, stream);
 }
 
 thd_status_t thd_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_seqlens,
                                     const int32_t* cu_seqlens_padded, int32_t num_docs, int64_t T, int32_t cp_size,
-                                    int32_t mtp_depth, int32_t fill, int32_t* labels, uint8_t* loss_mask,
+                                    int32_t mtp_depth, int32_t fill, const int32_t* next_token,
+                                    const uint8_t* has_next, int32_t* labels, uint8_t* loss_mask,
                                     uint8_t* valid_mask, int32_t* d_status, cudaStream_t stream) {
+  if ((next_token == nullptr) != (has_next == nullptr)) return THD_ERR_INVALID_ARG;
   if (!route_args_ok(T, cp_size) || num_docs < 0 || num_docs > kMaxRows - 1 || mtp_depth < 0 || mtp_depth > 64 ||
       !cu_seqlens || !cu_seqlens_padded || !d_status)
     return THD_ERR_INVALID_ARG;
   if (T > 0 && (!tokens || !labels || !loss_mask || !valid_mask)) return THD_ERR_INVALID_ARG;
   return launch_roll_labels_zigzag(tokens, cu_seqlens, cu_seqlens_padded, num_docs, static_cast<int32_t>(T),
-                                   cp_size, mtp_depth, fill, labels, loss_mask, valid_mask, d_status, stream);
+                                   cp_size, mtp_depth, fill, next_token, has_next, labels, loss_mask, valid_mask,
+                                   d_status, stream);
 }
 
 size_t thd_pack_docs_workspace_bytes(int32_t B, int64_t S) {
@@ -194,10 +199,12 @@ size_t thd_pack_docs_workspace_bytes(int32_t B, int64_t S) {
 }
 
 thd_status_t thd_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod_id, int32_t trim_raw_pad,
-                           int32_t raw_pad_id, int32_t align, int32_t pad_id, int32_t* tokens_out,
-                           int64_t tokens_capacity, int32_t* cu_seqlens, int32_t* cu_seqlens_padded,
+                           int32_t raw_pad_id, int32_t align, int32_t pad_id, const int32_t* row_next,
+                           int32_t* tokens_out, int64_t tokens_capacity, int32_t* cu_seqlens,
+                           int32_t* cu_seqlens_padded, int32_t* next_token, uint8_t* has_next,
                            int64_t docs_capacity, int64_t* counts, void* workspace, size_t workspace_bytes,
                            int32_t* d_status, cudaStream_t stream) {
+  if ((next_token == nullptr) != (has_next == nullptr) || (row_next && !has_next)) return THD_ERR_INVALID_ARG;
   if (B < 0 || B > kMaxRawRows || S < 0 || S > kMaxRows || align < 1 || tokens_capacity < 0 ||
       docs_capacity < 1 || !cu_seqlens || !cu_seqlens_padded || !counts || !d_status)
     return THD_ERR_INVALID_ARG;
@@ -205,9 +212,9 @@ thd_status_t thd_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod
   if (B > 0 && (!workspace || workspace_bytes < thd_pack_docs_workspace_bytes(B, S) ||
                 reinterpret_cast<uintptr_t>(workspace) % 8 != 0))
     return THD_ERR_INVALID_ARG;
-  return launch_pack_docs(raw, B, S, eod_id, trim_raw_pad ? 1 : 0, raw_pad_id, align, pad_id, tokens_out,
-                          tokens_capacity, cu_seqlens, cu_seqlens_padded, docs_capacity, counts,
-                          static_cast<int64_t*>(workspace), d_status, stream);
+  return launch_pack_docs(raw, B, S, eod_id, trim_raw_pad ? 1 : 0, raw_pad_id, align, pad_id, row_next, tokens_out,
+                          tokens_capacity, cu_seqlens, cu_seqlens_padded, next_token, has_next, docs_capacity,
+                          counts, static_cast<int64_t*>(workspace), d_status, stream);
 }
 
 thd_status_t thd_status_clear(int32_t* d_status, cudaStream_t stream) {

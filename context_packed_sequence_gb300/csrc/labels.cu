@@ -18,10 +18,42 @@ namespace {
 constexpr int kLabelThreads = 512;
 constexpr int kSmemBudget = 48 * 1024;
 
+// Optional continuation of a document cut by the end of its sample (the
+// sample's extra token, "Packed Sequence 与上下文并行" section 1.3): when
+// has[i], document i's token stream is its valid tokens followed by tok[i].
+struct NextTokens {
+  const int32_t* tok;
+  const uint8_t* has;
+};
+
+// Targets of global row g (document i, valid end e) written at position out:
+// depth k takes tokens[g+1+k] while inside the document, the document's next
+// token exactly one past its end, else `fill` with mask 0.
+__device__ __forceinline__ void write_targets(const int32_t* __restrict__ tokens, NextTokens next, int32_t i,
+                                              int32_t g, int32_t out, int32_t e, int32_t depth, int32_t fill,
+                                              int32_t T, int32_t* __restrict__ labels,
+                                              uint8_t* __restrict__ lmask) {
+  const bool cont = next.has != nullptr && next.has[i] != 0;
+  for (int32_t k = 0; k <= depth; ++k) {
+    const int32_t t = g + 1 + k;
+    int32_t v = fill;
+    uint8_t ok = 0;
+    if (t < e) {
+      v = __ldg(tokens + t);
+      ok = 1;
+    } else if (t == e && cont) {
+      v = next.tok[i];
+      ok = 1;
+    }
+    labels[static_cast<int64_t>(k) * T + out] = v;
+    lmask[static_cast<int64_t>(k) * T + out] = ok;
+  }
+}
+
 template <bool SMEM_CU>
 __global__ void __launch_bounds__(kLabelThreads)
 roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
-                   int32_t n, int32_t T, int32_t depth, int32_t fill, int32_t* __restrict__ labels,
+                   int32_t n, int32_t T, int32_t depth, int32_t fill, NextTokens next, int32_t* __restrict__ labels,
                    uint8_t* __restrict__ lmask, uint8_t* __restrict__ valid, int32_t* status) {
   extern __shared__ int32_t smem[];
   const int32_t* unused;
@@ -68,12 +100,7 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
     if (p < end) {
       const int32_t e = cu[i] + (cu_v[i + 1] - cu_v[i]);  // end of the document's valid tokens
       valid[p] = p < e ? 1 : 0;
-      for (int32_t k = 0; k <= depth; ++k) {
-        const int32_t t = p + 1 + k;
-        const bool ok = t < e;
-        labels[static_cast<int64_t>(k) * T + p] = ok ? __ldg(tokens + t) : fill;
-        lmask[static_cast<int64_t>(k) * T + p] = ok ? 1 : 0;
-      }
+      write_targets(tokens, next, i, p, p, e, depth, fill, T, labels, lmask);
     }
   }
 }
@@ -84,7 +111,7 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
 template <bool SMEM_CU>
 __global__ void __launch_bounds__(kLabelThreads)
 roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
-                          int32_t n, int32_t T, CpMath m, FastDiv divS, int32_t depth, int32_t fill,
+                          int32_t n, int32_t T, CpMath m, FastDiv divS, int32_t depth, int32_t fill, NextTokens next,
                           int32_t* __restrict__ labels, uint8_t* __restrict__ lmask, uint8_t* __restrict__ valid,
                           int32_t* status) {
   extern __shared__ int32_t smem[];
@@ -119,12 +146,7 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
     if (t.u < end) {
       const int32_t e = cu[t.doc] + (cu_v[t.doc + 1] - cu_v[t.doc]);
       valid[t.u] = t.g < e ? 1 : 0;
-      for (int32_t k = 0; k <= depth; ++k) {
-        const int32_t tt = t.g + 1 + k;
-        const bool ok = tt < e;
-        labels[static_cast<int64_t>(k) * T + t.u] = ok ? __ldg(tokens + tt) : fill;
-        lmask[static_cast<int64_t>(k) * T + t.u] = ok ? 1 : 0;
-      }
+      write_targets(tokens, next, t.doc, t.g, t.u, e, depth, fill, T, labels, lmask);
     }
   }
 }
@@ -132,8 +154,10 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
 }  // namespace
 
 thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu, int32_t n,
-                                       int32_t T, int32_t cp, int32_t depth, int32_t fill, int32_t* labels,
-                                       uint8_t* lmask, uint8_t* valid, int32_t* status, cudaStream_t s) {
+                                       int32_t T, int32_t cp, int32_t depth, int32_t fill, const int32_t* next_tok,
+                                       const uint8_t* has_next, int32_t* labels, uint8_t* lmask, uint8_t* valid,
+                                       int32_t* status, cudaStream_t s) {
+  const NextTokens next{next_tok, has_next};
   size_t bytes = static_cast<size_t>(2) * (n + 1) * sizeof(int32_t);
   bool in_smem = bytes <= static_cast<size_t>(kSmemBudget);
   int64_t grid = (static_cast<int64_t>(T) + kLabelThreads - 1) / kLabelThreads;
@@ -145,10 +169,10 @@ thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_
   const FastDiv divS = make_fast_div(S > 0 ? S : 1);
   if (in_smem)
     roll_labels_zigzag_kernel<true><<<static_cast<unsigned>(grid), kLabelThreads, bytes, s>>>(
-        tokens, cu_v, cu, n, T, m, divS, depth, fill, labels, lmask, valid, status);
+        tokens, cu_v, cu, n, T, m, divS, depth, fill, next, labels, lmask, valid, status);
   else
     roll_labels_zigzag_kernel<false><<<static_cast<unsigned>(grid), kLabelThreads, 0, s>>>(
-        tokens, cu_v, cu, n, T, m, divS, depth, fill, labels, lmask, valid, status);
+        tokens, cu_v, cu, n, T, m, divS, depth, fill, next, labels, lmask, valid, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
@@ -158,8 +182,10 @@ thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_
 }
 
 thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu,
-                                int32_t n, int32_t T, int32_t depth, int32_t fill, int32_t* labels,
-                                uint8_t* lmask, uint8_t* valid, int32_t* status, cudaStream_t s) {
+                                int32_t n, int32_t T, int32_t depth, int32_t fill, const int32_t* next_tok,
+                                const uint8_t* has_next, int32_t* labels, uint8_t* lmask, uint8_t* valid,
+                                int32_t* status, cudaStream_t s) {
+  const NextTokens next{next_tok, has_next};
   size_t bytes = static_cast<size_t>(2) * (n + 1) * sizeof(int32_t);
   bool in_smem = bytes <= static_cast<size_t>(kSmemBudget);
   int64_t grid = (static_cast<int64_t>(T) + kLabelThreads - 1) / kLabelThreads;
@@ -168,10 +194,10 @@ thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, cons
   if (grid < 1) grid = 1;
   if (in_smem)
     roll_labels_kernel<true><<<static_cast<unsigned>(grid), kLabelThreads, bytes, s>>>(
-        tokens, cu_v, cu, n, T, depth, fill, labels, lmask, valid, status);
+        tokens, cu_v, cu, n, T, depth, fill, next, labels, lmask, valid, status);
   else
     roll_labels_kernel<false><<<static_cast<unsigned>(grid), kLabelThreads, 0, s>>>(
-        tokens, cu_v, cu, n, T, depth, fill, labels, lmask, valid, status);
+        tokens, cu_v, cu, n, T, depth, fill, next, labels, lmask, valid, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);

@@ -265,8 +265,9 @@ pack_chunk_stats_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int6
 
 __global__ void __launch_bounds__(kChunkThreads)
 pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64_t* ve_arr, int32_t align,
-                       int32_t pad_id, const int64_t* stats, int32_t* tokens, int64_t tok_cap, int32_t* cu_v,
-                       int32_t* cu, int64_t docs_cap, int64_t* counts, int32_t* status) {
+                       int32_t pad_id, const int64_t* stats, const int32_t* row_next, int32_t* tokens,
+                       int64_t tok_cap, int32_t* cu_v, int32_t* cu, int32_t* next_tok, uint8_t* has_next,
+                       int64_t docs_cap, int64_t* counts, int32_t* status) {
   __shared__ int64_t tmp[32];
   __shared__ int64_t carry[4];  // last end before this chunk in its row, first doc index, output offset
   if (block_status_set(status)) return;
@@ -365,6 +366,13 @@ pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64
       for (int64_t zz = L; zz < P; ++zz) tokens[out + zz] = pad_id;
       cu_v[doc + 1] = static_cast<int32_t>(v_before + t + 1);
       cu[doc + 1] = static_cast<int32_t>(out + P);
+      if (has_next) {
+        // the row's extra token continues its last document when that
+        // document reaches the row's end without an EOD
+        const bool cont = row_next != nullptr && v != eod && ve == g.S;
+        has_next[doc] = cont ? 1 : 0;
+        next_tok[doc] = cont ? row_next[b] : 0;
+      }
       ++doc;
       out += P;
       pe = t;
@@ -413,9 +421,10 @@ size_t pack_docs_chunked_workspace(int32_t B, int64_t S) {
 }
 
 thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t trim,
-                              int32_t raw_pad, int32_t align, int32_t pad_id, int32_t* tokens,
-                              int64_t tok_cap, int32_t* cu_v, int32_t* cu, int64_t docs_cap,
-                              int64_t* counts, int64_t* ws, int32_t* status, cudaStream_t s) {
+                              int32_t raw_pad, int32_t align, int32_t pad_id, const int32_t* row_next,
+                              int32_t* tokens, int64_t tok_cap, int32_t* cu_v, int32_t* cu, int32_t* next_tok,
+                              uint8_t* has_next, int64_t docs_cap, int64_t* counts, int64_t* ws, int32_t* status,
+                              cudaStream_t s) {
   cudaError_t e;
   if (B == 0 || S == 0) {
     // no tokens: no documents, T = 0
@@ -447,8 +456,9 @@ thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t 
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
-  pack_chunk_emit_kernel<<<grid, kChunkThreads, 0, s>>>(raw, g, eod, ve, align, pad_id, stats, tokens, tok_cap,
-                                                        cu_v, cu, docs_cap, counts, status);
+  pack_chunk_emit_kernel<<<grid, kChunkThreads, 0, s>>>(raw, g, eod, ve, align, pad_id, stats, row_next, tokens,
+                                                        tok_cap, cu_v, cu, next_tok, has_next, docs_cap, counts,
+                                                        status);
   if ((e = cudaGetLastError()) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

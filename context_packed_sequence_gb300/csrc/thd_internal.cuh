@@ -359,17 +359,21 @@ thd_status_t launch_copy(CopyKind kind, const void* src, void* dst, int64_t row_
 thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes, bool seq_to_head,
                             int32_t* status, cudaStream_t s);
 thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu,
-                                int32_t n, int32_t T, int32_t depth, int32_t fill, int32_t* labels,
-                                uint8_t* lmask, uint8_t* valid, int32_t* status, cudaStream_t s);
-// chunked packing (workspace: pack_docs_chunked_workspace bytes, 8-byte aligned)
-size_t pack_docs_chunked_workspace(int32_t B, int64_t S);
+                                int32_t n, int32_t T, int32_t depth, int32_t fill, const int32_t* next_tok,
+                                const uint8_t* has_next, int32_t* labels, uint8_t* lmask, uint8_t* valid,
+                                int32_t* status, cudaStream_t s);
 thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu, int32_t n,
-                                       int32_t T, int32_t cp, int32_t depth, int32_t fill, int32_t* labels,
-                                       uint8_t* lmask, uint8_t* valid, int32_t* status, cudaStream_t s);
+                                       int32_t T, int32_t cp, int32_t depth, int32_t fill, const int32_t* next_tok,
+                                       const uint8_t* has_next, int32_t* labels, uint8_t* lmask, uint8_t* valid,
+                                       int32_t* status, cudaStream_t s);
+// chunked packing (workspace: pack_docs_chunked_workspace bytes, 8-byte aligned); row_next, next_tok
+// and has_next are optional (all null: no extra tokens)
+size_t pack_docs_chunked_workspace(int32_t B, int64_t S);
 thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t trim,
-                              int32_t raw_pad, int32_t align, int32_t pad_id, int32_t* tokens,
-                              int64_t tok_cap, int32_t* cu_v, int32_t* cu, int64_t docs_cap,
-                              int64_t* counts, int64_t* ws, int32_t* status, cudaStream_t s);
+                              int32_t raw_pad, int32_t align, int32_t pad_id, const int32_t* row_next,
+                              int32_t* tokens, int64_t tok_cap, int32_t* cu_v, int32_t* cu, int32_t* next_tok,
+                              uint8_t* has_next, int64_t docs_cap, int64_t* counts, int64_t* ws, int32_t* status,
+                              cudaStream_t s);
 // one block per raw row (workspace: 4 int64 per row)
 thd_status_t launch_pack_docs_rows(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t trim,
                                    int32_t raw_pad, int32_t align, int32_t pad_id, int32_t* tokens,

@@ -237,14 +237,20 @@ thd_status_t thd_ulysses_swap(const void *src, void *dst, int64_t T, int32_t cp_
  *  labels             device int32[mtp_depth+1][T]
  *  loss_mask          device uint8[mtp_depth+1][T]
  *  valid_mask         device uint8[T]
+ *  next_token, has_next  device int32[num_docs], uint8[num_docs], both NULL or
+ *                     both given: when has_next[i], document i continues with
+ *                     next_token[i] after its last valid token (a sample's
+ *                     extra token, "Packed Sequence 与上下文并行" section 1.3),
+ *                     so the target exactly one past e_i is next_token[i]
+ *                     (mask 1); thd_pack_docs produces both arrays.
  * Device checks, in order: padded cu (start, monotone, total), unpadded cu
  * (start, monotone), every unpadded length <= its padded length.
  */
 thd_status_t thd_roll_labels(const int32_t *tokens, const int32_t *cu_seqlens,
                              const int32_t *cu_seqlens_padded, int32_t num_docs, int64_t T,
-                             int32_t mtp_depth, int32_t fill, int32_t *labels,
-                             uint8_t *loss_mask, uint8_t *valid_mask, int32_t *d_status,
-                             cudaStream_t stream);
+                             int32_t mtp_depth, int32_t fill, const int32_t *next_token,
+                             const uint8_t *has_next, int32_t *labels, uint8_t *loss_mask,
+                             uint8_t *valid_mask, int32_t *d_status, cudaStream_t stream);
 
 /*
  * thd_roll_labels written directly in the zigzag layout of cp_size ranks:
@@ -260,9 +266,10 @@ thd_status_t thd_roll_labels(const int32_t *tokens, const int32_t *cu_seqlens,
  */
 thd_status_t thd_roll_labels_zigzag(const int32_t *tokens, const int32_t *cu_seqlens,
                                     const int32_t *cu_seqlens_padded, int32_t num_docs, int64_t T,
-                                    int32_t cp_size, int32_t mtp_depth, int32_t fill, int32_t *labels,
-                                    uint8_t *loss_mask, uint8_t *valid_mask, int32_t *d_status,
-                                    cudaStream_t stream);
+                                    int32_t cp_size, int32_t mtp_depth, int32_t fill,
+                                    const int32_t *next_token, const uint8_t *has_next,
+                                    int32_t *labels, uint8_t *loss_mask, uint8_t *valid_mask,
+                                    int32_t *d_status, cudaStream_t stream);
 
 /*
  * Pack raw rows into one padded THD sequence ("Packed Sequence 与上下文并行",
@@ -274,8 +281,14 @@ thd_status_t thd_roll_labels_zigzag(const int32_t *tokens, const int32_t *cu_seq
  * tokens_out followed by ((-L) mod align) copies of pad_id.
  *
  *  raw                device int32[B][S]
+ *  row_next           device int32[B] or NULL: each row's extra token (the
+ *                     sample's next token, section 1.3); requires has_next
  *  tokens_out         device int32[tokens_capacity]
  *  cu_seqlens, cu_seqlens_padded   device int32[docs_capacity]
+ *  next_token, has_next  device int32/uint8[docs_capacity], or both NULL: per
+ *                     document, has_next = 1 and next_token = row_next[b] when
+ *                     it is row b's last document, reaches the row's end and
+ *                     does not end with EOD; else 0 (for thd_roll_labels)
  *  counts             device int64[2]: {num_docs, T} on completion
  *  workspace          device, >= thd_pack_docs_workspace_bytes(B, S) bytes,
  *                     8-byte aligned; scratch between the kernels (one int64
@@ -290,8 +303,9 @@ thd_status_t thd_roll_labels_zigzag(const int32_t *tokens, const int32_t *cu_seq
 size_t thd_pack_docs_workspace_bytes(int32_t B, int64_t S);
 thd_status_t thd_pack_docs(const int32_t *raw, int32_t B, int64_t S, int32_t eod_id,
                            int32_t trim_raw_pad, int32_t raw_pad_id, int32_t align,
-                           int32_t pad_id, int32_t *tokens_out, int64_t tokens_capacity,
-                           int32_t *cu_seqlens, int32_t *cu_seqlens_padded,
+                           int32_t pad_id, const int32_t *row_next, int32_t *tokens_out,
+                           int64_t tokens_capacity, int32_t *cu_seqlens,
+                           int32_t *cu_seqlens_padded, int32_t *next_token, uint8_t *has_next,
                            int64_t docs_capacity, int64_t *counts, void *workspace,
                            size_t workspace_bytes, int32_t *d_status, cudaStream_t stream);
 
@@ -308,7 +322,8 @@ thd_status_t thd_pack_docs(const int32_t *raw, int32_t B, int64_t S, int32_t eod
  * allocating routine.
  *
  * Arguments, results and errors are those of thd_pack_docs, minus the
- * workspace.  The workspace is a fixed array compiled into the library
+ * workspace and the optional extra-token arguments (row_next, next_token,
+ * has_next), which this entry point does not take.  The workspace is a fixed array compiled into the library
  * (THD_PACK_NOALLOC_MAX_ROWS rows x 32 bytes = 128 KiB), held by every GPU
  * that loads the library until the process exits:
  *  - B > THD_PACK_NOALLOC_MAX_ROWS returns THD_ERR_SCRATCH_LIMIT at once and

@@ -369,7 +369,7 @@ def validate_label_args(cu_v, cu, T, depth):
                                 f"sequence {i}: valid length exceeds padded length")
 
 
-def roll_labels(tokens, cu_v, cu, depth, fill=0):
+def roll_labels(tokens, cu_v, cu, depth, fill=0, doc_next=None):
     """labels[k][p], loss_mask[k][p] for k = 0..depth, and valid[p].
 
     Position p of document i (cu[i] <= p < cu[i+1]) is valid when
@@ -379,14 +379,23 @@ def roll_labels(tokens, cu_v, cu, depth, fill=0):
     the document's last valid token into padding or into the next document
     ([PSCP] 1.3, 1.6).  Otherwise the label is ``fill`` and the mask 0 -- in
     particular at the EOD position itself ([PSCP] 3.8).
+
+    doc_next (optional, one entry per document, None or a token id): a
+    document cut by the end of its sample continues with the sample's extra
+    token ([PSCP] 1.3, ``last_extra_token``).  Its token stream is then the
+    valid tokens followed by that one token, so the target p+1+k == e_i is
+    doc_next[i] (mask 1) and only targets beyond it are ``fill``.
     """
     T = len(tokens)
     validate_label_args(cu_v, cu, T, depth)
+    if doc_next is not None and len(doc_next) != len(cu) - 1:
+        raise ThdValueError(INVALID_ARG, "doc_next needs one entry per document")
     labels = [[fill] * T for _ in range(depth + 1)]
     lmask = [[0] * T for _ in range(depth + 1)]
     valid = [0] * T
     for i in range(len(cu) - 1):
         e = cu[i] + (cu_v[i + 1] - cu_v[i])
+        nxt = None if doc_next is None else doc_next[i]
         for p in range(cu[i], cu[i + 1]):
             valid[p] = 1 if p < e else 0
             for k in range(depth + 1):
@@ -394,10 +403,13 @@ def roll_labels(tokens, cu_v, cu, depth, fill=0):
                 if t < e:
                     labels[k][p] = tokens[t]
                     lmask[k][p] = 1
+                elif t == e and nxt is not None:
+                    labels[k][p] = nxt
+                    lmask[k][p] = 1
     return labels, lmask, valid
 
 
-def roll_labels_zigzag(tokens, cu_v, cu, cp, depth, fill=0):
+def roll_labels_zigzag(tokens, cu_v, cu, cp, depth, fill=0, doc_next=None):
     """roll_labels, then the zigzag slicing of every output ([PSCP] 2.4 slices
     tokens, labels, loss mask and valid mask with the same index): position
     r*S + j holds the values of global row partition_indices(cu, T, cp, r)[j].
@@ -405,7 +417,7 @@ def roll_labels_zigzag(tokens, cu_v, cu, cp, depth, fill=0):
     Checks: the route's checks for (cu, T, cp) first, then the label checks."""
     T = len(tokens)
     validate_route_args(cu, T, cp, ZIGZAG_TO_CONTIGUOUS)
-    labels, lmask, valid = roll_labels(tokens, cu_v, cu, depth, fill)
+    labels, lmask, valid = roll_labels(tokens, cu_v, cu, depth, fill, doc_next)
     idx = partition_indices(cu, T, cp, -1)
     return ([[row[g] for g in idx] for row in labels],
             [[row[g] for g in idx] for row in lmask],
@@ -416,7 +428,7 @@ def roll_labels_zigzag(tokens, cu_v, cu, cp, depth, fill=0):
 # pack raw rows into one padded THD sequence ([PSCP] 2.2, 3.2-3.4)
 # --------------------------------------------------------------------------
 
-def pack_docs(raw, eod_id, align, pad_id=0, raw_pad_id=None):
+def pack_docs(raw, eod_id, align, pad_id=0, raw_pad_id=None, row_next=None):
     """Split each raw row into documents and flatten them with alignment padding.
 
     raw: list of B rows of token ids.  A row's valid region ends after its last
@@ -425,12 +437,17 @@ def pack_docs(raw, eod_id, align, pad_id=0, raw_pad_id=None):
     after the last EOD is a document as well; documents never span rows.  Each
     document of length L is padded with ``pad_id`` to L + ((-L) mod align).
 
-    Returns (tokens, cu_seqlens, cu_seqlens_padded).
+    Returns (tokens, cu_seqlens, cu_seqlens_padded); with ``row_next`` (one
+    extra token per row, the sample's ``last_extra_token`` of [PSCP] 1.3)
+    also doc_next: per document, the extra token of its row when the document
+    is that row's last one, reaches the row's end (no trailing pad) and does
+    not end with EOD, else None.
     """
     if align < 1:
         raise ThdValueError(INVALID_ARG, f"align must be >= 1, got {align}")
     docs = []
-    for row in raw:
+    doc_next = []
+    for b, row in enumerate(raw):
         ve = len(row)
         if raw_pad_id is not None:
             ve = 0
@@ -442,9 +459,12 @@ def pack_docs(raw, eod_id, align, pad_id=0, raw_pad_id=None):
             cur.append(row[t])
             if row[t] == eod_id:
                 docs.append(cur)
+                doc_next.append(None)
                 cur = []
         if cur:
             docs.append(cur)
+            continued = row_next is not None and ve == len(row)
+            doc_next.append(row_next[b] if continued else None)
     cu_v = [0]
     cu = [0]
     tokens = []
@@ -455,4 +475,6 @@ def pack_docs(raw, eod_id, align, pad_id=0, raw_pad_id=None):
         cu.append(cu[-1] + P)
         tokens.extend(d)
         tokens.extend([pad_id] * (P - L))
+    if row_next is not None:
+        return tokens, cu_v, cu, doc_next
     return tokens, cu_v, cu

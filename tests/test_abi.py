@@ -91,8 +91,13 @@ def test_host_checks_return_before_any_launch(lib):
     assert lib.thd_swap(fake, fake + 8, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG  # overlap
     assert lib.thd_swap(fake, fake + 4096, 0, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
     assert lib.thd_swap(fake, fake + 4096, 16, None, None, None) == L.ERR_INVALID_ARG
-    assert lib.thd_roll_labels(fake, fake, fake, 3, 24, -1, 0, fake, fake, fake, fake, None) == L.ERR_INVALID_ARG
-    assert lib.thd_pack_docs(fake, 2, 8, 99, 0, 0, 0, 0, fake, 16, fake, fake, 4, fake, fake, 64, fake,
-                             None) == L.ERR_INVALID_ARG   # align 0
+    assert lib.thd_roll_labels(fake, fake, fake, 3, 24, -1, 0, None, None, fake, fake, fake, fake,
+                               None) == L.ERR_INVALID_ARG   # depth -1
+    assert lib.thd_roll_labels(fake, fake, fake, 3, 24, 0, 0, fake, None, fake, fake, fake, fake,
+                               None) == L.ERR_INVALID_ARG   # next_token without has_next
+    assert lib.thd_pack_docs(fake, 2, 8, 99, 0, 0, 0, 0, None, fake, 16, fake, fake, None, None, 4, fake, fake,
+                             64, fake, None) == L.ERR_INVALID_ARG   # align 0
+    assert lib.thd_pack_docs(fake, 2, 8, 99, 0, 0, 4, 0, fake, fake, 16, fake, fake, None, None, 4, fake, fake,
+                             64, fake, None) == L.ERR_INVALID_ARG   # row_next without has_next
     assert lib.thd_pack_docs_workspace_bytes(8, 4096) == 8 * 8 + 8 * 2 * 32
     assert lib.thd_status_clear(None, None) == L.ERR_INVALID_ARG

@@ -358,6 +358,45 @@ def test_labels_never_cross_documents(depth):
         assert labels == ref_l and lmask == ref_m
 
 
+def test_extra_token_hand_example():
+    """A sample of S=6 tokens plus one extra token ([PSCP] 1.3): the document
+    the sample end cuts off gets the extra token as its last label."""
+    raw = [[1, 2, E, 3, 4, 5], [7, 8, 9, E, 10, E]]
+    tokens, cu_v, cu, doc_next = oracle.pack_docs(raw, E, align=1, row_next=[6, 11])
+    assert doc_next == [None, 6, None, None]          # row 1 ends with EOD: 11 starts a new document
+    labels, lmask, _ = oracle.roll_labels(tokens, cu_v, cu, 1, fill=-1, doc_next=doc_next)
+    assert labels[0] == [2, E, -1, 4, 5, 6, 8, 9, E, -1, E, -1]
+    assert lmask[0] == [1, 1, 0, 1, 1, 1, 1, 1, 1, 0, 1, 0]
+    assert labels[1] == [E, -1, -1, 5, 6, -1, 9, E, -1, -1, -1, -1]
+    # without the extra tokens the cut document's last label is masked, as before
+    assert oracle.roll_labels(tokens, cu_v, cu, 0, fill=-1)[0][0][5] == -1
+
+
+def test_extra_token_matches_rolling_each_sample():
+    """Second reading, as the page describes it: roll every sample left by one
+    with its extra token appended, then mask the EOD positions.  Depth 0 must
+    agree with the per-document definition, padded or not."""
+    rng = np.random.default_rng(21)
+    for trial in range(60):
+        B, S = int(rng.integers(1, 5)), int(rng.integers(1, 30))
+        raw = rng.integers(1, 20, size=(B, S))
+        raw[rng.random((B, S)) < 0.2] = E
+        raw = raw.tolist()
+        extra = [int(v) for v in rng.integers(1, 20, size=B)]
+        align = int(rng.choice([1, 2, 4]))
+        tokens, cu_v, cu, doc_next = oracle.pack_docs(raw, E, align, pad_id=-1, row_next=extra)
+        labels, lmask, valid = oracle.roll_labels(tokens, cu_v, cu, 0, fill=-9, doc_next=doc_next)
+        # packed position of row b, column t: documents are laid out row by row
+        got = []
+        for i in range(len(cu) - 1):
+            got.extend(labels[0][p] for p in range(cu[i], cu[i] + cu_v[i + 1] - cu_v[i]))
+        want = []
+        for b in range(B):
+            rolled = raw[b][1:] + [extra[b]]
+            want.extend(-9 if raw[b][t] == E else rolled[t] for t in range(S))
+        assert got == want
+
+
 def test_label_validation():
     with pytest.raises(O.ThdValueError) as e:
         oracle.roll_labels([1, 2, 3, 4], [0, 5], [0, 4], 0)

@@ -368,6 +368,39 @@ def test_roll_labels_zigzag_parity(cp, depth):
         assert got[2].cpu().tolist() == want[2]
 
 
+def test_extra_tokens_pack_and_labels():
+    """Rows with one extra token each: packing reports which documents it
+    continues, and both label kernels take it as the target one past the
+    document's end."""
+    rng = np.random.default_rng(31)
+    for trial in range(6):
+        B, S = int(rng.integers(1, 6)), int(rng.integers(1, 6000))
+        raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+        raw[rng.random((B, S)) < float(rng.choice([0.001, 0.05]))] = 7
+        if trial % 2:
+            raw[0, -1] = 7                      # a row ending exactly at EOD
+        extra = rng.integers(100, 200, size=B).astype(np.int32)
+        trim = trial % 3 == 0
+        if trim:
+            raw[-1, S // 2:] = 0                # trailing pad: no continuation for that row
+        align, cp = 8, 4
+        tok_o, cu_v_o, cu_o, nxt_o = oracle.pack_docs(raw.tolist(), 7, align, pad_id=0,
+                                                       raw_pad_id=0 if trim else None, row_next=extra.tolist())
+        tok, cu_v, cu, nt, hn = thd.pack_docs(torch.from_numpy(raw).cuda(), 7, align, pad_id=0,
+                                              raw_pad_id=0 if trim else None,
+                                              row_next=torch.from_numpy(extra).cuda())
+        assert tok.cpu().tolist() == tok_o and cu.cpu().tolist() == cu_o and cu_v.cpu().tolist() == cu_v_o
+        assert hn.cpu().tolist() == [int(v is not None) for v in nxt_o]
+        assert [v for v, h in zip(nt.cpu().tolist(), hn.cpu().tolist()) if h] == [v for v in nxt_o if v is not None]
+        for depth in (0, 2):
+            want = oracle.roll_labels(tok_o, cu_v_o, cu_o, depth, fill=-3, doc_next=nxt_o)
+            got = thd.roll_labels(tok, cu_v, cu, depth, -3, next_token=nt, has_next=hn)
+            assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
+            want_z = oracle.roll_labels_zigzag(tok_o, cu_v_o, cu_o, cp, depth, fill=-3, doc_next=nxt_o)
+            got_z = thd.roll_labels_zigzag(tok, cu_v, cu, cp, depth, -3, next_token=nt, has_next=hn)
+            assert [g.cpu().tolist() for g in got_z] == [list(w) for w in want_z]
+
+
 def test_pack_docs_worked_example_and_corners():
     E = 99
     cases = [

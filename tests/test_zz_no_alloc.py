@@ -42,9 +42,9 @@ def _with_workspace(lib, raw, eod, align, pad_id, trim, raw_pad):
     B, S = raw.shape
     tok, cu_v, cu, counts, st = _outputs(B, S, align, raw.device)
     ws = torch.empty(max(lib.thd_pack_docs_workspace_bytes(B, S), 8), dtype=torch.uint8, device=raw.device)
-    code = lib.thd_pack_docs(raw.data_ptr(), B, S, eod, trim, raw_pad, align, pad_id, tok.data_ptr(), tok.numel(),
-                             cu_v.data_ptr(), cu.data_ptr(), cu.numel(), counts.data_ptr(), ws.data_ptr(),
-                             ws.numel(), st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    code = lib.thd_pack_docs(raw.data_ptr(), B, S, eod, trim, raw_pad, align, pad_id, None, tok.data_ptr(),
+                             tok.numel(), cu_v.data_ptr(), cu.data_ptr(), None, None, cu.numel(), counts.data_ptr(),
+                             ws.data_ptr(), ws.numel(), st.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert code == L.OK
     return _result(tok, cu_v, cu, counts, st)
 
