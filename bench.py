@@ -489,7 +489,7 @@ def run_thd(args, rank, world, local):
     return result, dict(x=x, T=T, cu=cu_d, w=w, row_bytes=row_bytes)
 
 
-def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes, steps=6):
+def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes, steps=12):
     """End to end through the public API with host buffers.  Every step copies
     its input (x and the boundaries) from pinned host memory to the device,
     builds both routes, runs the layers' swap pairs and copies the result back

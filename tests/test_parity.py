@@ -297,6 +297,60 @@ def test_guard_rows_untouched():
     assert torch.equal(out, x[r.src_of_dst.long()])
 
 
+def test_guard_bytes_around_route_and_labels_untouched():
+    """Route arrays bound inside a larger poisoned buffer, and label outputs
+    inside poisoned buffers: nothing outside them is written."""
+    import ctypes
+    from context_packed_sequence_gb300 import _lib as L
+    lib = L.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    cu = _bounds(W.random_lengths(8, 60, 4, 11, 0.1))
+    T, cp, guard = cu[-1], 4, 4096
+    cu_d = _cu_tensor(cu)
+    nbytes = lib.thd_route_bytes(T, cp)
+    blob = torch.full((nbytes + 2 * guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    for d in (Z2C, C2Z):
+        c = L.ThdRoute()
+        assert lib.thd_route_bind(ctypes.byref(c), blob.data_ptr() + guard, nbytes, T, cp, d) == L.OK
+        st = thd.new_status()
+        assert lib.thd_route_build(cu_d.data_ptr(), len(cu) - 1, T, cp, d, ctypes.byref(c), st.data_ptr(),
+                                   stream) == L.OK
+        thd.check_status(st)
+        assert bool((blob[:guard] == 0x5A).all()) and bool((blob[guard + nbytes:] == 0x5A).all())
+
+    cu_v = _cu_tensor(_bounds([max(0, cu[i + 1] - cu[i] - 3) for i in range(len(cu) - 1)]))
+    tokens = torch.arange(T, dtype=torch.int32, device="cuda")
+    depth, pad = 2, 32
+    for fn, extra in ((lib.thd_roll_labels, ()), (lib.thd_roll_labels_zigzag, (cp,))):
+        lab = torch.full(((depth + 1) * T + 2 * pad,), -11, dtype=torch.int32, device="cuda")
+        msk = torch.full(((depth + 1) * T + 2 * pad,), 0xEE, dtype=torch.uint8, device="cuda")
+        val = torch.full((T + 2 * pad,), 0xEE, dtype=torch.uint8, device="cuda")
+        st = thd.new_status()
+        assert fn(tokens.data_ptr(), cu_v.data_ptr(), cu_d.data_ptr(), len(cu) - 1, T, *extra, depth, -1, None,
+                  None, lab.data_ptr() + 4 * pad, msk.data_ptr() + pad, val.data_ptr() + pad, st.data_ptr(),
+                  stream) == L.OK
+        thd.check_status(st)
+        n = (depth + 1) * T
+        assert bool((lab[:pad] == -11).all()) and bool((lab[pad + n:] == -11).all())
+        assert bool((msk[:pad] == 0xEE).all()) and bool((msk[pad + n:] == 0xEE).all())
+        assert bool((val[:pad] == 0xEE).all()) and bool((val[pad + T:] == 0xEE).all())
+
+
+def test_route_fuzz_many_cp():
+    """Random packings (empty documents included) for cp up to 64, both
+    directions in one launch, against the oracle."""
+    rng = np.random.default_rng(2024)
+    for trial in range(40):
+        cp = int(rng.choice([1, 2, 3, 5, 6, 7, 12, 16, 24, 32, 48, 64]))
+        n = int(rng.integers(0, 40))
+        lens = [2 * cp * int(rng.integers(0, 6)) for _ in range(n)]
+        cu = _bounds(lens)
+        T = cu[-1]
+        f, b = _gpu_pair(cu, T, cp)
+        _assert_route(f, oracle.build_route(cu, T, cp, Z2C))
+        _assert_route(b, oracle.build_route(cu, T, cp, C2Z))
+
+
 def test_movedim_wrapper_and_cache():
     cu = _cu_tensor(_bounds(W.random_lengths(3, 20, 2, 6, 0.0)))
     T = int(cu[-1])
