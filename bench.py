@@ -541,6 +541,19 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
 
     run(2)
     torch.cuda.synchronize(device)
+
+    # the link alone: one pinned upload and one download of x, each timed on the copy stream
+    def link_gbs(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cs):
+            a.record(cs)
+            fn()
+            b.record(cs)
+        torch.cuda.synchronize(device)
+        return round(x.numel() * x.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9, 1)
+
+    h2d_gbs = link_gbs(lambda: xd[0].copy_(x_host, non_blocking=True))
+    d2h_gbs = link_gbs(lambda: out_host[0].copy_(xd[0], non_blocking=True))
     barrier(world, device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(ks)
@@ -557,7 +570,8 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
             "h2d_bytes_per_step": int(x.numel() * x.element_size() + cu_d.numel() * 4),
             "d2h_bytes_per_step": int(x.numel() * x.element_size()),
             "ms_per_step": round(ms / steps, 3), "steps": steps,
-            "overlap": "uploads/downloads on a copy stream, double buffered against compute"}
+            "overlap": "uploads/downloads on a copy stream, double buffered against compute",
+            "link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
 # ---------------------------------------------------------------------------
