@@ -313,7 +313,8 @@ def run_thd(args, rank, world, local):
     barrier(world, device)
     clock_rec = clocks.stop() if clocks is not None else None
     step_ms_local = ev_step[0].elapsed_time(ev_step[-1])
-    swap_ms_total = sum(a.elapsed_time(b) for a, b in ev_sw)
+    per_step_swap_ms = [a.elapsed_time(b) for a, b in ev_sw]
+    swap_ms_total = sum(per_step_swap_ms)
     code = thd.status_read(status)
     if code != 0:
         raise RuntimeError(f"device status {code} in the timed region")
@@ -323,6 +324,14 @@ def run_thd(args, rank, world, local):
     value = bytes_all / (total_ms / 1e3) / 1e9
     swap_us = swap_ms_total * 1e3 / (2 * layers * n_ev)
     achieved = swap_bytes / (swap_us * 1e-6) / 1e9
+    # per-step average swap time: its median and 10th / 90th percentiles
+    per_swap = sorted(v * 1e3 / (2 * layers) for v in per_step_swap_ms)
+
+    def pct(q):
+        return round(per_swap[min(len(per_swap) - 1, int(q * (len(per_swap) - 1) + 0.5))], 2)
+
+    swap_dist = {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9), "unit": "us per launch",
+                 "over": f"{n_ev} steps of {2 * layers} launches"}
 
     # route build alone: CUDA events around each build, the GPU kept busy so
     # host launch latency is not counted; median of 50
@@ -465,6 +474,7 @@ def run_thd(args, rank, world, local):
         "rows_per_s": round(T * 2 * layers * n_ev * world / (total_ms / 1e3), 1),
         "route_build_us": route_us,
         "swap_us_per_launch": round(swap_us, 2),
+        "swap_us_distribution": swap_dist,
         "frac_of_spec_8tbs": round(achieved / SPEC_HBM_GBS, 4),
         "roofline": {
             "bound": "hbm",
@@ -615,6 +625,7 @@ def run_cpu_baseline(w, budget_s):
         if el >= budget_s:
             break
     return {"value": round(done * swap_bytes / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "host_cpus": os.cpu_count(),
             "sample": f"{done} oracle swap(s) of the full {w.name} workload (T={T}, {w.row_bytes} B rows), "
                       f"each = per-token route build of one direction + pack/all-to-all/scatter row by row, "
                       f"pure Python on 1 thread, {el:.1f} s"}
@@ -654,7 +665,7 @@ def run_reference(args, rank, world):
         "config": {"workload": w.name, "description": w.description, "cp_size": w.cp, "T": T,
                    "row_bytes": w.row_bytes},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "host_cpus": os.cpu_count(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
