@@ -120,14 +120,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def copy_engine_digest():
+    """sha256 of the swap kernel's sources: copy.cu followed by tma.cuh."""
+    h = hashlib.sha256()
+    for name in ("copy.cu", "tma.cuh"):
+        with open(os.path.join(ROOT, "context_packed_sequence_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def swap_traffic_record():
     """dram bytes per swap launch from the committed ncu summary, or None when
-    the summary is missing or the copy kernel's source changed since."""
+    the summary is missing or the copy kernel's sources changed since."""
     path = os.path.join(ROOT, "profiles", "bulk_copy_swap_lognorm128k.md")
-    src = os.path.join(ROOT, "context_packed_sequence_gb300", "csrc", "copy.cu")
     try:
         text = open(path).read()
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        digest = copy_engine_digest()
     except OSError:
         return None
     fields = {}
@@ -135,7 +143,7 @@ def swap_traffic_record():
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    if fields.get("copy.cu sha256") != digest:
+    if fields.get("copy engine sha256") != digest:
         return None
     try:
         return int(fields["dram bytes per launch"])
@@ -433,7 +441,11 @@ def run_thd(args, rank, world, local):
         to_seq = uly_time(1, y, x)
         if thd.status_read(status) != 0:
             raise RuntimeError("device status set by the Ulysses exchange")
-        uly = {"piece_bytes": row_bytes // cp, "seq_to_head_us": round(to_head, 2),
+        piece = row_bytes // cp
+        # the library's rule (copy.cu / ulysses_tile.cu): pieces that are
+        # multiples of 16 bytes below 1 KiB take the tile transpose
+        engine = "ulysses_tile_kernel" if cp > 1 and piece % 16 == 0 and piece < 1024 else "row engine"
+        uly = {"piece_bytes": piece, "engine": engine, "seq_to_head_us": round(to_head, 2),
                "head_to_seq_us": round(to_seq, 2),
                "gbs": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3, 1),
                "frac_of_measured": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3 / peak_gbs, 4)}

@@ -19,7 +19,12 @@
 //  * unit engine (everything else: narrow, odd-sized or unaligned rows): the
 //    linear side is walked as a flat array of 16-, 4- or 1-byte units, 32*U
 //    consecutive units per warp step, (row, column) kept incrementally.
+//
+// The Ulysses exchange takes the tile transpose of ulysses_tile.cu when its
+// head-group pieces are multiples of 16 bytes below 1 KiB, these engines
+// otherwise.
 #include "thd_internal.cuh"
+#include "tma.cuh"
 
 namespace thd {
 namespace {
@@ -226,48 +231,6 @@ thd_status_t run(const void* src, void* dst, int32_t rows, int64_t row_bytes, Ma
 // ---- the bulk (TMA) engine -------------------------------------------------
 
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr int kWaitLimit = 1 << 20;  // try_wait polls before a wait gives up
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-// Bounded wait for the phase with the given parity; false when it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (int it = 0; it < kWaitLimit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(sdst)),
-               "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// all but the newest bulk group of this thread have finished reading shared memory
-__device__ __forceinline__ void bulk_wait_read_all_but_one() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Lane `lane` starts a run in `starts`; the run ends before the next lane that
 // starts another run or is not in `members`.
@@ -295,12 +258,7 @@ bulk_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, BulkGeom 
   uint32_t* masks = reinterpret_cast<uint32_t*>(bars + NST);
   int32_t* mrows = reinterpret_cast<int32_t*>(masks + NST);
   const int lane = threadIdx.x;
-  // Launched with programmatic stream serialization: this block may start
-  // while the previous kernel on the stream is still finishing.  Nothing is
-  // read or written before that kernel has completed and its writes are
-  // visible; then the next such kernel may start its own blocks.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_wait_then_release();  // launched with programmatic dependent launch
   // one read, broadcast: the warp must take this exit together
   if (__shfl_sync(kFull, lane == 0 ? status_load(status) : 0, 0) != 0) return;
   const int64_t b = blockIdx.x, G = gridDim.x;
@@ -310,7 +268,7 @@ bulk_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, BulkGeom 
   const int64_t rb = g.row_bytes;
   if (lane == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   __syncwarp();
   bool bad = false;
@@ -534,6 +492,8 @@ thd_status_t dispatch_unit(const void* src, void* dst, int32_t rows, int64_t row
 thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes, bool seq_to_head,
                             int32_t* status, cudaStream_t s) {
   if (T == 0) return THD_OK;
+  if (ulysses_tiles_apply(src, dst, T, cp, row_bytes))  // small head groups: tile transpose
+    return launch_ulysses_tiles(src, dst, T, cp, row_bytes, seq_to_head, status, s);
   const UlyssesMap map{T, cp, seq_to_head, make_fast_div(seq_to_head ? T : cp)};
   return dispatch_unit<UlyssesMap, false>(src, dst, T * cp, row_bytes / cp, map, status, s);
 }

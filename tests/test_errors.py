@@ -138,6 +138,23 @@ def test_status_is_sticky_until_cleared():
     assert r.src_of_dst.cpu().tolist() == oracle.build_route([0, 8, 16], 16, 2, Z2C).src_of_dst
 
 
+@pytest.mark.parametrize("cp,heads,head_bytes", [(16, 16, 32), (8, 32, 256)])
+def test_ulysses_skips_when_status_is_set(cp, heads, head_bytes):
+    """A set status word makes the exchange a no-op (tile transpose and bulk
+    row engine alike); after clearing it the exchange runs."""
+    x = torch.randint(0, 256, (64, heads, head_bytes), dtype=torch.uint8, device="cuda")
+    out = torch.full((cp, 64, heads // cp, head_bytes), 7, dtype=torch.uint8, device="cuda")
+    st = thd.new_status()
+    thd.route_build(torch.tensor([0, 6, 16], dtype=torch.int32, device="cuda"), 16, 2, Z2C, status=st)
+    thd.ulysses_swap(x, cp, thd.SEQ_TO_HEAD, out=out, status=st)
+    assert thd.status_read(st) == L.ERR_LEN_NOT_DIVISIBLE
+    assert bool((out == 7).all())
+    thd.status_clear(st)
+    thd.ulysses_swap(x, cp, thd.SEQ_TO_HEAD, out=out, status=st)
+    assert thd.status_read(st) == L.OK
+    assert torch.equal(thd.ulysses_swap(out, cp, thd.HEAD_TO_SEQ), x)
+
+
 @pytest.mark.parametrize("width", [8, 128, 4096, 12288])
 def test_corrupted_route_index_is_range_checked(width):
     """An out-of-range entry is skipped by the kernel's own check (the access

@@ -228,11 +228,17 @@ def test_unaligned_buffers_take_the_narrow_path():
 
 
 @pytest.mark.parametrize("cp,T,heads,head_bytes", [
-    (2, 64, 8, 64),     # 256-byte pieces: bulk engine
-    (4, 96, 8, 64),     # 128-byte pieces: unit engine, 16-byte units
-    (8, 64, 32, 256),   # 1 KiB pieces, as the 128K workloads
-    (2, 30, 2, 6),      # 6-byte pieces: byte units
-    (1, 16, 4, 32),
+    (2, 64, 8, 64),          # 256-byte pieces: tile transpose, one partial tile
+    (4, 96, 8, 64),          # 128-byte pieces: tile transpose
+    (8, 64, 32, 256),        # 1 KiB pieces, as the 128K workloads: bulk row engine
+    (2, 30, 2, 6),           # 6-byte pieces: byte units
+    (1, 16, 4, 32),          # cp = 1: a plain copy
+    (16, 19984, 16, 32),     # 32-byte pieces: several tiles per block, ragged last tile
+    (3, 1503, 3, 48),        # cp = 3, pieces of three 16-byte units, ragged
+    (2, 10, 2, 16),          # 16-byte pieces, one partial tile
+    (32, 64, 32, 1008),      # rows of 31.5 KiB: one token per tile
+    (64, 64, 64, 1008),      # a tile would not fit in shared memory: bulk row engine
+    (64, 128, 64, 16),       # cp = 64: each issuing lane takes two runs
 ])
 def test_ulysses_parity(cp, T, heads, head_bytes):
     rng = np.random.default_rng(cp * 100 + T)
@@ -247,6 +253,29 @@ def test_ulysses_parity(cp, T, heads, head_bytes):
     assert np.array_equal(y.cpu().numpy().reshape(cp * T, -1), want)
     assert np.array_equal(back.cpu().numpy().reshape(T, -1), oracle.ulysses_swap(want, cp, oracle.HEAD_TO_SEQ))
     assert torch.equal(back, x)
+
+
+@pytest.mark.parametrize("cp,T,piece", [(16, 19984, 32), (3, 1503, 48), (8, 424, 512)])
+def test_ulysses_guard_bytes_untouched(cp, T, piece):
+    """The tile transpose writes exactly its output: 256 guard bytes on each
+    side of the destination keep their pattern in both directions."""
+    lib = thd._lib.load()
+    row = cp * piece
+    x = torch.randint(0, 256, (T, row), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = thd.new_status()
+    heads = torch.full((T * row + 512,), 0x5A, dtype=torch.uint8, device="cuda")
+    seq = torch.full((T * row + 512,), 0x5A, dtype=torch.uint8, device="cuda")
+    assert lib.thd_ulysses_swap(x.data_ptr(), heads.data_ptr() + 256, T, cp, row, thd.SEQ_TO_HEAD,
+                                st.data_ptr(), s) == 0
+    assert lib.thd_ulysses_swap(heads.data_ptr() + 256, seq.data_ptr() + 256, T, cp, row, thd.HEAD_TO_SEQ,
+                                st.data_ptr(), s) == 0
+    thd.check_status(st)
+    for buf in (heads, seq):
+        assert bool((buf[:256] == 0x5A).all()) and bool((buf[256 + T * row:] == 0x5A).all())
+    want = oracle.ulysses_swap(x.cpu().numpy(), cp, oracle.SEQ_TO_HEAD)
+    assert np.array_equal(heads[256:256 + T * row].cpu().numpy().reshape(cp * T, piece), want)
+    assert torch.equal(seq[256:256 + T * row].view(T, row), x)
 
 
 def test_zigzag_to_ulysses_and_back():
@@ -527,6 +556,30 @@ def test_full_size_workloads(name):
     w = W.BY_NAME[name]
     cu = _bounds(W.doc_lengths(name))
     _full_size_swap_check(cu, w.cp, w.hidden, w.seed)
+
+
+@pytest.mark.parametrize("name", ["lognorm128k", "longtail128k", "stress16"])
+def test_full_size_ulysses(name, sample=4096):
+    """The Ulysses exchange of the full hidden states: sampled tokens against
+    the oracle, every byte by the round trip.  stress16 splits 512-byte rows
+    16 ways (32-byte pieces, the tile transpose); the 128K workloads have
+    1 KiB pieces (the bulk row engine)."""
+    w = W.BY_NAME[name]
+    T = sum(W.doc_lengths(name))
+    x = W.payload_device(w.seed, T, w.hidden, "cuda")
+    heads = x.shape[1]
+    st = thd.new_status()
+    y = thd.ulysses_swap(x, w.cp, thd.SEQ_TO_HEAD, status=st)
+    back = thd.ulysses_swap(y, w.cp, thd.HEAD_TO_SEQ, status=st)
+    thd.check_status(st)
+    rows = np.sort(np.random.default_rng(w.seed).choice(T, size=sample - sample % w.cp, replace=False))
+    idx = torch.from_numpy(rows).cuda().long()
+    xs = x[idx].contiguous().view(torch.uint8).reshape(len(rows), -1).cpu().numpy()
+    want = oracle.ulysses_swap(xs, w.cp, oracle.SEQ_TO_HEAD).reshape(w.cp, len(rows), -1)
+    got = y[:, idx].contiguous().view(torch.uint8).reshape(w.cp, len(rows), -1).cpu().numpy()
+    assert y.shape[2] == heads // w.cp
+    assert np.array_equal(got, want)
+    assert torch.equal(back, x)
 
 
 def test_full_size_pipeline():
