@@ -144,6 +144,7 @@ __device__ __forceinline__ void advance(int64_t& q, int32_t& c, int64_t dq, int3
 template <typename Unit, class Map, bool SCATTER>
 __global__ void __launch_bounds__(kCopyThreads, kCopyBlocksPerSm)
 copy_rows_kernel(const Unit* __restrict__ src, Unit* __restrict__ dst, Walk w, Map map, int32_t* status) {
+  pdl_wait_then_release();
   if (status_load(status) != 0) return;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -217,9 +218,9 @@ thd_status_t run(const void* src, void* dst, int32_t rows, int64_t row_bytes, Ma
   const int64_t step = grid * per_block;  // units all warps advance per step
   w.step_q = step / w.upr;
   w.step_c = static_cast<int32_t>(step % w.upr);
-  copy_rows_kernel<Unit, Map, SCATTER><<<static_cast<unsigned>(grid), kCopyThreads, 0, s>>>(
-      static_cast<const Unit*>(src), static_cast<Unit*>(dst), w, map, status);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(copy_rows_kernel<Unit, Map, SCATTER>, dim3(static_cast<unsigned>(grid)),
+                                   kCopyThreads, 0, s, static_cast<const Unit*>(src), static_cast<Unit*>(dst), w,
+                                   map, status);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
@@ -442,19 +443,8 @@ thd_status_t launch_bulk(const BulkPlan& p, const void* src, void* dst, Map map,
     // programmatic dependent launch: back-to-back copies overlap one's
     // launch and ramp-up with the previous one's tail (about 2.3 us per
     // launch on GB300); the kernel waits for its predecessor before any access
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(32);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, bulk_copy_kernel<NST, Map, SCATTER>, static_cast<const char*>(src),
-                           static_cast<char*>(dst), p.g, map, status);
-    if (e == cudaSuccess) e = cudaGetLastError();
+    e = launch_pdl(bulk_copy_kernel<NST, Map, SCATTER>, dim3(static_cast<unsigned>(grid)), 32, smem, s,
+                   static_cast<const char*>(src), static_cast<char*>(dst), p.g, map, status);
   }
   if (e != cudaSuccess) {
     record_cuda_error(e);

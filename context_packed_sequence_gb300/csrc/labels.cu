@@ -57,6 +57,7 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
                    uint8_t* __restrict__ lmask, uint8_t* __restrict__ valid, int32_t* status) {
   extern __shared__ int32_t smem[];
   const int32_t* unused;
+  pdl_wait_then_release();
   if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
   stage_cu(cu_v_g, n, smem + (n + 1), SMEM_CU);
   const int32_t* cu = SMEM_CU ? smem : cu_g;
@@ -116,6 +117,7 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
                           int32_t* status) {
   extern __shared__ int32_t smem[];
   const int32_t* unused;
+  pdl_wait_then_release();
   if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
   stage_cu(cu_v_g, n, smem + (n + 1), SMEM_CU);
   const int32_t* cu = SMEM_CU ? smem : cu_g;
@@ -167,13 +169,12 @@ thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_
   const int32_t S = T / cp;
   const CpMath m = make_cp_math(cp);
   const FastDiv divS = make_fast_div(S > 0 ? S : 1);
-  if (in_smem)
-    roll_labels_zigzag_kernel<true><<<static_cast<unsigned>(grid), kLabelThreads, bytes, s>>>(
-        tokens, cu_v, cu, n, T, m, divS, depth, fill, next, labels, lmask, valid, status);
-  else
-    roll_labels_zigzag_kernel<false><<<static_cast<unsigned>(grid), kLabelThreads, 0, s>>>(
-        tokens, cu_v, cu, n, T, m, divS, depth, fill, next, labels, lmask, valid, status);
-  cudaError_t e = cudaGetLastError();
+  const dim3 blocks(static_cast<unsigned>(grid));
+  const cudaError_t e =
+      in_smem ? launch_pdl(roll_labels_zigzag_kernel<true>, blocks, kLabelThreads, bytes, s, tokens, cu_v, cu, n, T,
+                           m, divS, depth, fill, next, labels, lmask, valid, status)
+              : launch_pdl(roll_labels_zigzag_kernel<false>, blocks, kLabelThreads, 0, s, tokens, cu_v, cu, n, T, m,
+                           divS, depth, fill, next, labels, lmask, valid, status);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
@@ -192,13 +193,12 @@ thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, cons
   int64_t cap = static_cast<int64_t>(sm_count()) * 2;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  if (in_smem)
-    roll_labels_kernel<true><<<static_cast<unsigned>(grid), kLabelThreads, bytes, s>>>(
-        tokens, cu_v, cu, n, T, depth, fill, next, labels, lmask, valid, status);
-  else
-    roll_labels_kernel<false><<<static_cast<unsigned>(grid), kLabelThreads, 0, s>>>(
-        tokens, cu_v, cu, n, T, depth, fill, next, labels, lmask, valid, status);
-  cudaError_t e = cudaGetLastError();
+  const dim3 blocks(static_cast<unsigned>(grid));
+  const cudaError_t e =
+      in_smem ? launch_pdl(roll_labels_kernel<true>, blocks, kLabelThreads, bytes, s, tokens, cu_v, cu, n, T, depth,
+                           fill, next, labels, lmask, valid, status)
+              : launch_pdl(roll_labels_kernel<false>, blocks, kLabelThreads, 0, s, tokens, cu_v, cu, n, T, depth, fill,
+                           next, labels, lmask, valid, status);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kPackThreads)
 pack_stats_kernel(const int32_t* raw, int64_t S, int32_t eod, int32_t trim, int32_t raw_pad,
                   int32_t align, int64_t* ws, int32_t* status) {
   __shared__ int64_t tmp[32];
+  pdl_wait_then_release();
   if (block_status_set(status)) return;
   const int64_t b = blockIdx.x;
   const int32_t* row = raw + b * S;
@@ -102,6 +103,7 @@ pack_emit_kernel(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t 
                  int32_t* tokens, int64_t tok_cap, int32_t* cu_v, int32_t* cu, int64_t docs_cap,
                  int64_t* counts, const int64_t* ws, int32_t* status) {
   __shared__ int64_t tmp[32];
+  pdl_wait_then_release();
   if (block_status_set(status)) return;
   const int64_t b = blockIdx.x;
   // where this row starts: sums over the rows before it, and the grand totals
@@ -214,6 +216,7 @@ struct ChunkGeom {
 __global__ void __launch_bounds__(kPackThreads)
 pack_row_ends_kernel(const int32_t* raw, int64_t S, int32_t raw_pad, int64_t* ve, int32_t* status) {
   __shared__ int64_t tmp[32];
+  pdl_wait_then_release();
   if (block_status_set(status)) return;
   const int64_t b = blockIdx.x;
   const int64_t v = row_valid_end(raw + b * S, S, 1, raw_pad, tmp);
@@ -226,6 +229,7 @@ __global__ void __launch_bounds__(kChunkThreads)
 pack_chunk_stats_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64_t* ve_arr, int32_t align,
                         int64_t* stats, int32_t* status) {
   __shared__ int64_t tmp[32];
+  pdl_wait_then_release();
   if (block_status_set(status)) return;
   const int64_t b = blockIdx.y, c = blockIdx.x;
   const int32_t* row = raw + b * g.S;
@@ -270,6 +274,7 @@ pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64
                        int64_t docs_cap, int64_t* counts, int32_t* status) {
   __shared__ int64_t tmp[32];
   __shared__ int64_t carry[4];  // last end before this chunk in its row, first doc index, output offset
+  pdl_wait_then_release();
   if (block_status_set(status)) return;
   const int64_t b = blockIdx.y, c = blockIdx.x, me = b * g.per_row + c;
   const int64_t key_span = g.S + 2;  // key = row * key_span + (last end + 1)
@@ -397,14 +402,13 @@ thd_status_t launch_pack_docs_rows(const int32_t* raw, int32_t B, int64_t S, int
     }
     return THD_OK;
   }
-  pack_stats_kernel<<<B, kPackThreads, 0, s>>>(raw, S, eod, trim, raw_pad, align, ws, status);
-  if ((e = cudaGetLastError()) != cudaSuccess) {
+  if ((e = launch_pdl(pack_stats_kernel, B, kPackThreads, 0, s, raw, S, eod, trim, raw_pad, align, ws, status)) !=
+      cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
-  pack_emit_kernel<<<B, kPackThreads, 0, s>>>(raw, B, S, eod, align, pad_id, tokens, tok_cap, cu_v, cu,
-                                              docs_cap, counts, ws, status);
-  if ((e = cudaGetLastError()) != cudaSuccess) {
+  if ((e = launch_pdl(pack_emit_kernel, B, kPackThreads, 0, s, raw, B, S, eod, align, pad_id, tokens, tok_cap, cu_v,
+                      cu, docs_cap, counts, ws, status)) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
@@ -444,22 +448,20 @@ thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t 
   int64_t* ve = trim ? ws : nullptr;
   int64_t* stats = ws + B;
   if (trim) {
-    pack_row_ends_kernel<<<B, kPackThreads, 0, s>>>(raw, S, raw_pad, ws, status);
-    if ((e = cudaGetLastError()) != cudaSuccess) {
+    if ((e = launch_pdl(pack_row_ends_kernel, B, kPackThreads, 0, s, raw, S, raw_pad, ws, status)) != cudaSuccess) {
       record_cuda_error(e);
       return THD_ERR_CUDA;
     }
   }
   const dim3 grid(static_cast<unsigned>(g.per_row), static_cast<unsigned>(B));
-  pack_chunk_stats_kernel<<<grid, kChunkThreads, 0, s>>>(raw, g, eod, ve, align, stats, status);
-  if ((e = cudaGetLastError()) != cudaSuccess) {
+  if ((e = launch_pdl(pack_chunk_stats_kernel, grid, kChunkThreads, 0, s, raw, g, eod,
+                      static_cast<const int64_t*>(ve), align, stats, status)) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
-  pack_chunk_emit_kernel<<<grid, kChunkThreads, 0, s>>>(raw, g, eod, ve, align, pad_id, stats, row_next, tokens,
-                                                        tok_cap, cu_v, cu, next_tok, has_next, docs_cap, counts,
-                                                        status);
-  if ((e = cudaGetLastError()) != cudaSuccess) {
+  if ((e = launch_pdl(pack_chunk_emit_kernel, grid, kChunkThreads, 0, s, raw, g, eod,
+                      static_cast<const int64_t*>(ve), align, pad_id, static_cast<const int64_t*>(stats), row_next,
+                      tokens, tok_cap, cu_v, cu, next_tok, has_next, docs_cap, counts, status)) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   int32_t* roff = cnt + cp * (cp + 1);        // [d][cp+1]: z->c receive offsets
   int32_t* cu_s = roff + cp * (cp + 1);
   const int32_t* unused;
+  pdl_wait_then_release();
   if (stage_cu_check_status(a.cu, n, cu_s, SMEM_CU, a.status, &unused)) return;
   const int32_t* cu = SMEM_CU ? cu_s : a.cu;
 
@@ -164,6 +165,7 @@ partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, CpMath m, FastDiv di
                  int32_t* out, int32_t* status) {
   extern __shared__ int32_t smem[];
   const int32_t* unused;
+  pdl_wait_then_release();
   if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
   const int32_t* cu = SMEM_CU ? smem : cu_g;
   int32_t code = block_check_cu(cu, n, T, 2 * m.cp, true);
@@ -214,22 +216,22 @@ thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t
   a.cu_in_smem = tables + cu_bytes <= static_cast<size_t>(kSmemBudget);
   size_t smem = tables + (a.cu_in_smem ? cu_bytes : 0);
   int grid = grid_for(T, kRouteThreads, 2);
+  cudaError_t e;
   if (a.cu_in_smem) {
     if (dirs == (kZC | kCZ))
-      route_build_kernel<kZC | kCZ, true><<<grid, kRouteThreads, smem, s>>>(a);
+      e = launch_pdl(route_build_kernel<kZC | kCZ, true>, grid, kRouteThreads, smem, s, a);
     else if (dirs == kZC)
-      route_build_kernel<kZC, true><<<grid, kRouteThreads, smem, s>>>(a);
+      e = launch_pdl(route_build_kernel<kZC, true>, grid, kRouteThreads, smem, s, a);
     else
-      route_build_kernel<kCZ, true><<<grid, kRouteThreads, smem, s>>>(a);
+      e = launch_pdl(route_build_kernel<kCZ, true>, grid, kRouteThreads, smem, s, a);
   } else {
     if (dirs == (kZC | kCZ))
-      route_build_kernel<kZC | kCZ, false><<<grid, kRouteThreads, smem, s>>>(a);
+      e = launch_pdl(route_build_kernel<kZC | kCZ, false>, grid, kRouteThreads, smem, s, a);
     else if (dirs == kZC)
-      route_build_kernel<kZC, false><<<grid, kRouteThreads, smem, s>>>(a);
+      e = launch_pdl(route_build_kernel<kZC, false>, grid, kRouteThreads, smem, s, a);
     else
-      route_build_kernel<kCZ, false><<<grid, kRouteThreads, smem, s>>>(a);
+      e = launch_pdl(route_build_kernel<kCZ, false>, grid, kRouteThreads, smem, s, a);
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
@@ -245,11 +247,10 @@ thd_status_t launch_partition(const int32_t* cu, int32_t n, int32_t T, int32_t c
   int grid = grid_for(rank < 0 ? T : S, kRouteThreads, 2);
   const CpMath m = make_cp_math(cp);
   const FastDiv divS = make_fast_div(S > 0 ? S : 1);
-  if (in_smem)
-    partition_kernel<true><<<grid, kRouteThreads, cu_bytes, s>>>(cu, n, T, m, divS, S, rank, out, status);
-  else
-    partition_kernel<false><<<grid, kRouteThreads, 0, s>>>(cu, n, T, m, divS, S, rank, out, status);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      in_smem ? launch_pdl(partition_kernel<true>, grid, kRouteThreads, cu_bytes, s, cu, n, T, m, divS, S, rank, out,
+                           status)
+              : launch_pdl(partition_kernel<false>, grid, kRouteThreads, 0, s, cu, n, T, m, divS, S, rank, out, status);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "thd.h"
+#include "tma.cuh"
 
 namespace thd {
 
@@ -345,6 +346,28 @@ struct OpMax {
 
 void record_cuda_error(cudaError_t e);
 int sm_count();
+
+// Every kernel of this library is launched with programmatic stream
+// serialization: it may be scheduled while the previous kernel on the stream
+// is still finishing, which hides the launch gap between back-to-back
+// kernels.  Each kernel's first statement is pdl_wait_then_release()
+// (tma.cuh), so it touches memory only after its predecessor has completed.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  return e == cudaSuccess ? cudaGetLastError() : e;
+}
 
 // launchers (one per translation unit); return THD_OK or THD_ERR_CUDA
 // dirs: bit 0 = zigzag->contiguous into zc, bit 1 = contiguous->zigzag into cz

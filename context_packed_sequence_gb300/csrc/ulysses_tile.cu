@@ -189,18 +189,8 @@ thd_status_t launch_tiles(const void* src, void* dst, const TileGeom& g, size_t 
     if (per_sm < 1) per_sm = 1;
     int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
     if (grid > g.tiles) grid = g.tiles;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kTileThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kernel, static_cast<const char*>(src), static_cast<char*>(dst), g, status);
-    if (e == cudaSuccess) e = cudaGetLastError();
+    e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), kTileThreads, smem, s, static_cast<const char*>(src),
+                   static_cast<char*>(dst), g, status);
   }
   if (e != cudaSuccess) {
     record_cuda_error(e);
