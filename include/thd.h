@@ -215,8 +215,11 @@ thd_status_t thd_scatter(const void *recv_buf, void *dst, int64_t row_bytes,
  *   THD_HEAD_TO_SEQ: the inverse.
  * With all ranks in one buffer the exchange is a block transpose.
  *  T          0 <= T, a multiple of cp_size, T*cp_size < 2^31.
- *  row_bytes  > 0, a multiple of cp_size; pieces of >= 256 bytes that are a
- *             multiple of 16 (16-byte aligned buffers) move by TMA bulk copies.
+ *  row_bytes  > 0, a multiple of cp_size.  With 16-byte aligned buffers and
+ *             pieces (row_bytes/cp_size) that are multiples of 16 bytes, the
+ *             exchange moves by TMA bulk copies: pieces below 1 KiB (cp_size
+ *             >= 2) as a tile transpose through shared memory, larger pieces
+ *             one by one; other shapes by 16-, 4- or 1-byte loads and stores.
  *  d_status   as for thd_swap.  A bad dir returns THD_ERR_BAD_DIRECTION.
  */
 thd_status_t thd_ulysses_swap(const void *src, void *dst, int64_t T, int32_t cp_size,
