@@ -95,11 +95,13 @@ struct A2AMap {
       s = (__ldg(ro + s + half) <= j) ? s + half : s;
       len -= half;
     }
-    int32_t m = j - __ldg(ro + s);
-    int32_t n = __ldg(in_split + s * cp + d);
-    int32_t off = __ldg(send_off + s * (cp + 1) + d);
+    // the route's entries are checked, not trusted: 64-bit so that corrupted
+    // values cannot wrap around the checks
+    const int64_t m = static_cast<int64_t>(j) - __ldg(ro + s);
+    const int32_t n = __ldg(in_split + s * cp + d);
+    const int32_t off = __ldg(send_off + s * (cp + 1) + d);
     if (m < 0 || m >= n || off < 0 || off + m >= S) return -1;
-    return s * S + off + m;
+    return s * S + off + static_cast<int32_t>(m);
   }
 };
 

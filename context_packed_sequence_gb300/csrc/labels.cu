@@ -34,14 +34,16 @@ __device__ __forceinline__ void write_targets(const int32_t* __restrict__ tokens
                                               int32_t T, int32_t* __restrict__ labels,
                                               uint8_t* __restrict__ lmask) {
   const bool cont = next.has != nullptr && next.has[i] != 0;
+  // depth k reads tokens[g+1+k] while k < room; comparing k with the room left
+  // keeps every sum below e, so nothing overflows when T is near INT32_MAX
+  const int32_t room = e - g - 1;
   for (int32_t k = 0; k <= depth; ++k) {
-    const int32_t t = g + 1 + k;
     int32_t v = fill;
     uint8_t ok = 0;
-    if (t < e) {
-      v = __ldg(tokens + t);
+    if (k < room) {
+      v = __ldg(tokens + g + 1 + k);
       ok = 1;
-    } else if (t == e && cont) {
+    } else if (k == room && cont) {
       v = next.tok[i];
       ok = 1;
     }
@@ -68,8 +70,8 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
     code = block_check_cu(cu_v, n, 0, 0, false);
     if (code == THD_OK) {
       int bad = 0;
-      for (int32_t i = threadIdx.x; i < n; i += blockDim.x)
-        if (cu_v[i + 1] - cu_v[i] > cu[i + 1] - cu[i]) bad = 1;
+      for (uint32_t i = threadIdx.x; i < static_cast<uint32_t>(n); i += blockDim.x)
+        if (cu_v[i + 1] - cu_v[i] > cu[i + 1] - cu[i]) bad = 1;  // both checked monotone from 0
       if (__syncthreads_or(bad)) code = THD_ERR_VALID_EXCEEDS_PADDED;
     }
   }
@@ -128,8 +130,8 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
     code = block_check_cu(cu_v, n, 0, 0, false);
     if (code == THD_OK) {
       int bad = 0;
-      for (int32_t i = threadIdx.x; i < n; i += blockDim.x)
-        if (cu_v[i + 1] - cu_v[i] > cu[i + 1] - cu[i]) bad = 1;
+      for (uint32_t i = threadIdx.x; i < static_cast<uint32_t>(n); i += blockDim.x)
+        if (cu_v[i + 1] - cu_v[i] > cu[i + 1] - cu[i]) bad = 1;  // both checked monotone from 0
       if (__syncthreads_or(bad)) code = THD_ERR_VALID_EXCEEDS_PADDED;
     }
   }

@@ -55,11 +55,12 @@ __device__ bool has_descent(const int32_t* cu, int32_t n, CpMath m, int32_t lo, 
     if (L == 0) continue;
     int32_t c = m.div2(L);
     // descents at b = cu[i] + k*c, k = cp+1 .. 2cp-1; need lo+1 <= b <= hi-1
-    int32_t a = lo + 1 - cu[i];
-    int32_t klo = a <= 0 ? cp + 1 : max(cp + 1, (a + c - 1) / c);
-    int32_t b = hi - 1 - cu[i];
+    // (ceil(a / c) as (a - 1) / c + 1: a + c - 1 could pass INT32_MAX)
+    const int32_t a = lo + 1 - cu[i];
+    const int32_t klo = a <= 0 ? cp + 1 : max(cp + 1, (a - 1) / c + 1);
+    const int32_t b = hi - 1 - cu[i];
     if (b < 0) continue;
-    int32_t khi = min(2 * cp - 1, b / c);
+    const int32_t khi = min(2 * cp - 1, b / c);
     if (klo <= khi) return true;
   }
   return false;

@@ -60,10 +60,14 @@ __device__ __forceinline__ int32_t block_check_cu(const int32_t* cu, int32_t n, 
   int mono_bad = 0, div_bad = 0;
   // a power-of-two multiple is tested with a mask (the usual 2*cp)
   const bool pow2 = mult > 0 && (mult & (mult - 1)) == 0;
-  for (int32_t i = threadIdx.x; i < n; i += blockDim.x) {
-    int32_t a = cu[i], b = cu[i + 1];
+  const uint32_t um = static_cast<uint32_t>(mult);
+  // unsigned counter and length: n may be close to INT32_MAX, and b - a of
+  // b >= a always fits 32 unsigned bits whatever the (unchecked) values are
+  for (uint32_t i = threadIdx.x; i < static_cast<uint32_t>(n); i += blockDim.x) {
+    const int32_t a = cu[i], b = cu[i + 1];
+    const uint32_t len = static_cast<uint32_t>(b) - static_cast<uint32_t>(a);
     if (b < a) mono_bad = 1;
-    else if (mult > 0 && (pow2 ? ((b - a) & (mult - 1)) : ((b - a) % mult)) != 0) div_bad = 1;
+    else if (mult > 0 && (pow2 ? (len & (um - 1)) : (len % um)) != 0) div_bad = 1;
   }
   int any_mono = __syncthreads_or(mono_bad);
   int any_div = __syncthreads_or(div_bad);
@@ -174,11 +178,13 @@ __device__ __forceinline__ int32_t doc_in(const int32_t* cu, int32_t lo, int32_t
 // distance), so following a position that only moves forward is cheap.
 __device__ __forceinline__ int32_t doc_from(const int32_t* cu, int32_t n, int32_t i, int32_t x) {
   int32_t step = 1;
-  while (i + step <= n && cu[i + step] <= x) {
+  // written so that nothing overflows for n up to INT32_MAX - 1: the step
+  // stops doubling at 2^30 and is compared with the distance left
+  while (step <= n - i && cu[i + step] <= x) {
     i += step;
-    step <<= 1;
+    if (step < (1 << 30)) step <<= 1;
   }
-  return doc_in(cu, i, min(i + step - 1, n), x);
+  return doc_in(cu, i, i + min(step - 1, n - i), x);
 }
 
 // The documents of a warp's 32 consecutive positions: one full search for
