@@ -207,6 +207,53 @@ def test_route_and_swaps_capture_in_a_cuda_graph():
     assert torch.equal(z, x)
 
 
+def test_full_step_captures_in_a_cuda_graph():
+    """Labels in both layouts, the route pair, bulk swaps and the Ulysses tile
+    transpose (whose launch sets its shared-memory size and asks for its
+    occupancy) captured in one graph and replayed twice.  Packing runs before
+    the capture: the caller reads T from it once to size the buffers."""
+    E, cp = 99, 2
+    raw = torch.tensor([[1, 2, 3, E, 4, 5, E, 0], [6, 7, 8, 9, 10, E, 0, 0]], dtype=torch.int32, device="cuda")
+    tok, cu_v, cu = thd.pack_docs(raw, E, 2 * cp)            # T known on the host once, outside capture
+    T = tok.numel()
+    x = torch.randint(0, 256, (T, 16, 32), dtype=torch.uint8, device="cuda")
+    st = thd.new_status()
+    fwd, bwd = thd.Route(T, cp, Z2C), thd.Route(T, cp, C2Z)
+    out = {}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def step():
+        thd.route_build_pair(cu, T, cp, status=st, routes=(fwd, bwd))
+        out["labels"] = thd.roll_labels(tok, cu_v, cu, 1, status=st)
+        out["zigzag_labels"] = thd.roll_labels_zigzag(tok, cu_v, cu, cp, 1, status=st)
+        out["y"] = thd.swap(x, fwd, status=st)
+        out["heads"] = thd.ulysses_swap(out["y"], cp, thd.SEQ_TO_HEAD, status=st)
+        out["seq"] = thd.ulysses_swap(out["heads"], cp, thd.HEAD_TO_SEQ, status=st)
+        out["back"] = thd.swap(out["seq"], bwd, status=st)
+
+    with torch.cuda.stream(s):
+        step()                                                 # warm-up outside capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+    for _ in range(2):
+        out["back"].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert thd.status_read(st) == L.OK
+        assert torch.equal(out["back"], x)
+    cu_l, cu_v_l, tok_l = cu.cpu().tolist(), cu_v.cpu().tolist(), tok.cpu().tolist()
+    o = oracle.build_route(cu_l, T, cp, Z2C)
+    assert torch.equal(out["y"].cpu(), x.cpu()[torch.tensor(o.src_of_dst)])
+    want = oracle.ulysses_swap(out["y"].cpu().numpy().reshape(T, -1), cp, oracle.SEQ_TO_HEAD)
+    assert (out["heads"].cpu().numpy().reshape(cp * T, -1) == want).all()
+    assert [t.cpu().tolist() for t in out["labels"]] == list(oracle.roll_labels(tok_l, cu_v_l, cu_l, 1))
+    assert [t.cpu().tolist() for t in out["zigzag_labels"]] == list(
+        oracle.roll_labels_zigzag(tok_l, cu_v_l, cu_l, cp, 1))
+
+
 def test_python_layer_makes_no_torch_sync():
     cu = torch.tensor([0, 16, 48], dtype=torch.int32, device="cuda")
     x = torch.randn(48, 32, device="cuda")
