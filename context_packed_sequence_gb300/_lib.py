@@ -11,6 +11,13 @@ import os
 from ctypes import POINTER, c_int32, c_int64, c_size_t, c_void_p, c_char_p
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libthd.so")
+# THD_CHECKED=1 in the environment: the debug build, whose kernels range-check
+# every row index they compute (built by `build --checked` / build())
+CHECKED_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libthd_checked.so")
+
+
+def lib_path() -> str:
+    return CHECKED_LIB_PATH if os.environ.get("THD_CHECKED", "0") == "1" else LIB_PATH
 
 # status codes (thd_status_t)
 OK = 0
@@ -110,11 +117,13 @@ def load():
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
+    path = lib_path()
+    if not os.path.exists(path):
         raise RuntimeError(
-            f"libthd.so is not built ({LIB_PATH}); run `python -m context_packed_sequence_gb300.build` "
-            "or `__graft_entry__.build()` -- there is no CPU fallback")
-    lib = ctypes.CDLL(LIB_PATH)
+            f"{os.path.basename(path)} is not built ({path}); run `python -m context_packed_sequence_gb300.build"
+            f"{' --checked' if path == CHECKED_LIB_PATH else ''}` or `__graft_entry__.build()` -- there is no CPU "
+            "fallback")
+    lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res

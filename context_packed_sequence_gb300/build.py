@@ -3,9 +3,12 @@
 Every ``csrc/*.cu`` translation unit is compiled in parallel into
 ``_build/thd/`` at the repository root, then linked into
 ``context_packed_sequence_gb300/libthd.so`` (CUDA runtime linked statically,
-so the library loads without any library path set up).
+so the library loads without any library path set up).  ``--checked`` builds
+the debug variant ``libthd_checked.so`` (``-DTHD_CHECKED=1``: every computed
+row index is range-checked in the kernels), which the package loads when
+``THD_CHECKED=1`` is set in the environment.
 
-    python -m context_packed_sequence_gb300.build
+    python -m context_packed_sequence_gb300.build [--checked]
 """
 
 from __future__ import annotations
@@ -22,6 +25,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "thd")
 LIB = os.path.join(PKG, "libthd.so")
+BUILD_CHECKED = os.path.join(ROOT, "_build", "thd_checked")
+LIB_CHECKED = os.path.join(PKG, "libthd_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -46,12 +51,14 @@ def _compile(args):
     return src, cmd, r
 
 
-def build(extra_flags=(), verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(extra_flags=(), verbose: bool = False, checked: bool = False) -> str:
+    build_dir, lib_path = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    flags = list(extra_flags) + (["-DTHD_CHECKED=1"] if checked else [])
+    os.makedirs(build_dir, exist_ok=True)
     jobs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        jobs.append((src, obj, list(extra_flags)))
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+        jobs.append((src, obj, flags))
     with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
         results = list(ex.map(_compile, jobs))
     failed = False
@@ -61,15 +68,16 @@ def build(extra_flags=(), verbose: bool = False) -> str:
         failed |= r.returncode != 0
     if failed:
         raise RuntimeError("libthd: compilation failed (see the nvcc output above)")
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[j[1] for j in jobs]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
         raise RuntimeError("libthd: link failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(extra_flags=sys.argv[1:], verbose=True))
+    args = sys.argv[1:]
+    print(build(extra_flags=[a for a in args if a != "--checked"], verbose=True, checked="--checked" in args))

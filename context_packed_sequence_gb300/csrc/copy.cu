@@ -115,12 +115,16 @@ struct UlyssesMap {
   bool seq_to_head;
   FastDiv div;  // by T (seq -> head) or by cp (head -> seq)
   __device__ __forceinline__ int32_t operator()(int32_t q) const {
+    int32_t v;
     if (seq_to_head) {  // destination piece (r, g) <- source piece (g, r)
       const int32_t r = div.div(q), g = q - r * T;
-      return g * cp + r;
+      v = g * cp + r;
+    } else {
+      const int32_t g = div.div(q), r = q - g * cp;  // destination (g, r) <- source (r, g)
+      v = r * T + g;
     }
-    const int32_t g = div.div(q), r = q - g * cp;  // destination (g, r) <- source (r, g)
-    return r * T + g;
+    // checked build: -1 makes the engines skip the piece and report it
+    return in_range(v, 0, static_cast<int64_t>(T) * cp, nullptr) ? v : -1;
   }
 };
 

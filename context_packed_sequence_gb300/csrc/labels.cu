@@ -100,8 +100,9 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
     const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
     const int32_t i = doc_in(cu, i_lo, i_hi, pc);
     doc = i_lo;
-    if (p < end) {
+    if (p < end && in_range(i, 0, n, status)) {
       const int32_t e = cu[i] + (cu_v[i + 1] - cu_v[i]);  // end of the document's valid tokens
+      if (!in_range(e, 0, static_cast<int64_t>(T) + 1, status)) continue;  // token reads stay below e
       valid[p] = p < e ? 1 : 0;
       write_targets(tokens, next, i, p, p, e, depth, fill, T, labels, lmask);
     }
@@ -147,8 +148,9 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
   for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
     const TileRow t = tile_row(cu, n, m, S, divS, static_cast<int32_t>(tile0) + lane,
                                static_cast<int32_t>(end) - 1, w);
-    if (t.u < end) {
+    if (t.u < end && in_range(t.doc, 0, n, status) && in_range(t.g, 0, T, status)) {
       const int32_t e = cu[t.doc] + (cu_v[t.doc + 1] - cu_v[t.doc]);
+      if (!in_range(e, 0, static_cast<int64_t>(T) + 1, status)) continue;  // token reads stay below e
       valid[t.u] = t.g < e ? 1 : 0;
       write_targets(tokens, next, t.doc, t.g, t.u, e, depth, fill, T, labels, lmask);
     }

@@ -173,13 +173,16 @@ pack_emit_kernel(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t 
         int64_t t = t0 + it;
         if (t >= ve) break;
         int32_t v = row[t];
-        tokens[out + (t - prev - 1)] = v;
+        if (in_range(out + (t - prev - 1), 0, t_all, status)) tokens[out + (t - prev - 1)] = v;
         if (v == eod || t == ve - 1) {
           int64_t L = t - prev;
           int64_t P = L + pad_of(L, align);
-          for (int64_t z = L; z < P; ++z) tokens[out + z] = pad_id;
-          cu_v[doc + 1] = static_cast<int32_t>(v_before + t + 1);
-          cu[doc + 1] = static_cast<int32_t>(out + P);
+          for (int64_t z = L; z < P; ++z)
+            if (in_range(out + z, 0, t_all, status)) tokens[out + z] = pad_id;
+          if (in_range(doc + 1, 1, d_all + 1, status)) {
+            cu_v[doc + 1] = static_cast<int32_t>(v_before + t + 1);
+            cu[doc + 1] = static_cast<int32_t>(out + P);
+          }
           ++doc;
           out += P;
           prev = t;
@@ -364,11 +367,13 @@ pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64
     const int64_t t = t0 + it;
     if (t >= hi) break;
     const int32_t v = row[t];
-    tokens[out + (t - pe - 1)] = v;
+    if (in_range(out + (t - pe - 1), 0, t_all, status)) tokens[out + (t - pe - 1)] = v;
     if (v == eod || t == ve - 1) {
       const int64_t L = t - pe;
       const int64_t P = L + pad_of(L, align);
-      for (int64_t zz = L; zz < P; ++zz) tokens[out + zz] = pad_id;
+      for (int64_t zz = L; zz < P; ++zz)
+        if (in_range(out + zz, 0, t_all, status)) tokens[out + zz] = pad_id;
+      if (!in_range(doc + 1, 1, d_all + 1, status)) break;
       cu_v[doc + 1] = static_cast<int32_t>(v_before + t + 1);
       cu[doc + 1] = static_cast<int32_t>(out + P);
       if (has_next) {

@@ -143,9 +143,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
     const TileRow t = tile_row(cu, n, m, S, divS, static_cast<int32_t>(tile0) + lane,
                                static_cast<int32_t>(end) - 1, w);
-    if (t.u < end) {
+    if (t.u < end && in_range(t.doc, 0, n, a.status) && in_range(t.g, 0, T, a.status)) {
       const int32_t d = divS.div(t.g);
       const int32_t pos = d * S + roff[d * (cp + 1) + t.r] + (t.j - cnt[t.r * (cp + 1) + d]);
+      if (!in_range(pos, d * static_cast<int64_t>(S), (d + 1) * static_cast<int64_t>(S), a.status)) continue;
       if (DIRS & kZC) {
         a.zc.src_of_dst[t.g] = t.u;
         a.zc.send_rows[t.u] = t.j;
@@ -185,7 +186,7 @@ partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, CpMath m, FastDiv di
   for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
     const int32_t k = static_cast<int32_t>(tile0) + lane;
     const TileRow t = tile_row(cu, n, m, S, divS, base + k, base + static_cast<int32_t>(end) - 1, w);
-    if (k < end) out[k] = t.g;
+    if (k < end && in_range(t.g, 0, T, status)) out[k] = t.g;
   }
 }
 

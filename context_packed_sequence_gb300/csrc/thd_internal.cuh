@@ -19,6 +19,23 @@ __device__ __forceinline__ int32_t status_load(const int32_t* st) {
   return st ? *reinterpret_cast<const volatile int32_t*>(st) : 0;
 }
 
+// Debug build (compiled with THD_CHECKED=1, loaded with THD_CHECKED=1 in the
+// environment): every row index a kernel computes in closed form is checked
+// against its range before it is used; a miss records THD_ERR_INDEX_RANGE and
+// the access is skipped.  The default build compiles the checks away: the
+// closed forms stay in range by construction on validated input.
+#if defined(THD_CHECKED) && THD_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+__device__ __forceinline__ bool in_range(int64_t v, int64_t lo, int64_t hi, int32_t* st) {
+  if (!kChecked || (v >= lo && v < hi)) return true;
+  if (st) atomicCAS(st, 0, static_cast<int32_t>(THD_ERR_INDEX_RANGE));
+  return false;
+}
+
 // Block-uniform "is the status word already set?": one thread reads, the
 // whole block sees the same answer, so kernels with barriers may return on it.
 __device__ __forceinline__ bool block_status_set(const int32_t* st) {

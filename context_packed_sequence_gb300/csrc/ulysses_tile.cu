@@ -94,6 +94,14 @@ ulysses_tile_kernel(const char* __restrict__ src, char* __restrict__ dst, TileGe
   // tile t covers tokens [t*R, t*R + rt)
   auto tile_start = [&](int i) { return static_cast<int64_t>(b + i * G) * g.R; };
   auto tile_rows = [&](int64_t g0) { return min(static_cast<int64_t>(g.R), g.T - g0); };
+  // checked build: every tile of this block lies inside [0, T), else the
+  // block moves nothing (no bulk copy has been issued yet)
+  if (kChecked) {
+    bool bad = false;
+    if (tid == 0)
+      for (int i = 0; i < n_my; ++i) bad |= !in_range(tile_start(i), 0, g.T, status);
+    if (__syncthreads_or(bad)) return;
+  }
 
   // warp 0 only: lane 0 arms the stage's barrier before any lane loads into it
   auto issue_load = [&](int i) {

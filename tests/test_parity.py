@@ -396,6 +396,9 @@ def test_movedim_wrapper_and_cache():
     cu.add_(0)                                                          # in-place write bumps _version
     assert cache.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is not r1
     assert cache.get(cu.clone(), T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is not r1
+    r2 = cache.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS)
+    assert cache.get(cu, T, 1, thd.ZIGZAG_TO_CONTIGUOUS) is not r2      # dynamic CP: another cp_size rebuilds
+    assert cache.get(cu, T, 2, thd.ZIGZAG_TO_CONTIGUOUS) is not r2      # ... and so does switching back
     assert thd.zigzag_contiguous_thd_swap(x, cu, 1, 0, seq_dim=1) is x  # cp == 1: nothing moves
     pre = thd.RouteCache()
     pre.prebuild(cu, T, 2)                                              # both directions, one launch
