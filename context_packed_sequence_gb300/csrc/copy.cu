@@ -25,6 +25,7 @@
 // otherwise.
 #include "thd_internal.cuh"
 #include "tma.cuh"
+#include "thd_debug.h"
 
 namespace thd {
 namespace {
@@ -239,6 +240,15 @@ thd_status_t run(const void* src, void* dst, int32_t rows, int64_t row_bytes, Ma
 
 constexpr uint32_t kFull = 0xffffffffu;
 
+// Checked build only: a one-shot request (thd_debug_stall_next_bulk_copy)
+// that block 0 of the next bulk copy arms 16 bytes no copy delivers, so its
+// first wait runs out and the timeout path runs for real.
+__device__ int g_stall_request;
+
+__device__ __forceinline__ void maybe_stall(int64_t i, uint64_t* bar) {
+  if (kChecked && i == 0 && blockIdx.x == 0 && atomicExch(&g_stall_request, 0) != 0) mbar_expect_tx(bar, 16);
+}
+
 // Lane `lane` starts a run in `starts`; the run ends before the next lane that
 // starts another run or is not in `members`.
 __device__ __forceinline__ int run_end(int lane, uint32_t starts, uint32_t members) {
@@ -309,6 +319,7 @@ bulk_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, BulkGeom 
       if (lane == 0) {
         masks[s] = vmask;
         mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(__popc(vmask)) * static_cast<uint32_t>(rb));
+        maybe_stall(i, &bars[s]);
       }
       __syncwarp();
       if (start) {
@@ -324,6 +335,7 @@ bulk_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, BulkGeom 
       mrows[s * 32] = m;
       if (m >= 0) {
         mbar_arrive_expect_tx(&bars[s], bytes);
+        maybe_stall(i, &bars[s]);
         const char* from = SCATTER ? src + q * rb + off : src + static_cast<int64_t>(m) * rb + off;
         bulk_load(st, from, bytes, &bars[s]);
       } else {
@@ -518,3 +530,17 @@ thd_status_t launch_copy(CopyKind kind, const void* src, void* dst, int64_t row_
 }
 
 }  // namespace thd
+
+#if defined(THD_CHECKED) && THD_CHECKED
+// Declared in include/thd_debug.h; exported by the checked build only.
+extern "C" thd_status_t thd_debug_stall_next_bulk_copy(cudaStream_t stream) {
+  const int one = 1;
+  const cudaError_t e =
+      cudaMemcpyToSymbolAsync(thd::g_stall_request, &one, sizeof(one), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) {
+    thd::record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  return THD_OK;
+}
+#endif

@@ -28,7 +28,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Raise the transaction count the current phase waits for (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
 // Bounded wait for the phase with the given parity; false when it gave up.
+// One poll of a phase that is not complete costs about 3 us on GB300, so a
+// wait gives up after about 3 s.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (int it = 0; it < kWaitLimit; ++it) {
     uint32_t done;

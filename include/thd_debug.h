@@ -1,0 +1,32 @@
+/*
+ * Debug entry points of libthd_checked.so, the debug build of libthd
+ * (compiled with THD_CHECKED=1; the default libthd.so does not export them).
+ * The pages have no counterpart: these exist to test the library's own
+ * failure handling without faulting the GPU.
+ */
+#ifndef THD_DEBUG_H
+#define THD_DEBUG_H
+
+#include "thd.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * One-shot: block 0 of the next TMA bulk copy launched by the library (a
+ * thd_swap / pack / scatter of rows of 256 bytes or more, or a Ulysses
+ * exchange of pieces of 1 KiB or more) waits on 16 bytes that no copy
+ * delivers.  Its bounded wait runs out (about 3 s), the block lets its other
+ * copies land, records THD_ERR_TIMEOUT in the call's d_status and returns;
+ * the rest of the copy completes normally and the context stays usable.
+ *  stream   the request is written to device memory in stream order.
+ * Returns THD_OK, or THD_ERR_CUDA (detail in thd_last_cuda_error()).
+ */
+thd_status_t thd_debug_stall_next_bulk_copy(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* THD_DEBUG_H */

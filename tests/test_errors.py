@@ -4,6 +4,9 @@ trap; downstream kernels must then write nothing.  Also: a corrupted route
 index is caught by the kernels' own range check, and route build plus swaps
 are captured in a CUDA graph, which any host synchronisation would break."""
 
+import ctypes
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -153,6 +156,45 @@ def test_ulysses_skips_when_status_is_set(cp, heads, head_bytes):
     thd.ulysses_swap(x, cp, thd.SEQ_TO_HEAD, out=out, status=st)
     assert thd.status_read(st) == L.OK
     assert torch.equal(thd.ulysses_swap(out, cp, thd.HEAD_TO_SEQ), x)
+
+
+@pytest.mark.parametrize("tokens_capacity,ok", [(15, False), (16, True), (64, True)])
+def test_pack_docs_reports_a_too_small_output(tokens_capacity, ok):
+    """Two documents of 4 and 2 tokens padded to multiples of 8 need 16 output
+    tokens: with room for 15 the device reports THD_ERR_CAPACITY and writes no
+    document; with 16 or more the packing matches the oracle."""
+    raw = [[1, 2, 3, 99, 4, 5]]
+    kw = dict(tokens_capacity=tokens_capacity)
+    if not ok:
+        with pytest.raises(thd.ThdError) as e:
+            thd.pack_docs(torch.tensor(raw, dtype=torch.int32, device="cuda"), 99, 8, **kw)
+        assert e.value.kind == "capacity"
+        return
+    tok, cu_v, cu = thd.pack_docs(torch.tensor(raw, dtype=torch.int32, device="cuda"), 99, 8, **kw)
+    want = oracle.pack_docs(raw, 99, 8)
+    assert (tok.cpu().tolist(), cu_v.cpu().tolist(), cu.cpu().tolist()) == tuple(want)
+
+
+@pytest.mark.skipif(os.environ.get("THD_CHECKED") != "1", reason="the debug request is in the checked build only")
+def test_bulk_wait_that_runs_out_reports_timeout():
+    """Block 0 of a bulk swap waits for 16 bytes that never come: its bounded
+    wait gives up (about 3 s), the block lets its other copies land and
+    records THD_ERR_TIMEOUT; the next swap on the same context is exact."""
+    lib = L.load()
+    stall = lib.thd_debug_stall_next_bulk_copy
+    stall.restype, stall.argtypes = ctypes.c_int, [ctypes.c_void_p]
+    cu = torch.tensor([0, 8, 20, 24], dtype=torch.int32, device="cuda")
+    r = thd.route_build(cu, 24, 2, Z2C)
+    x = torch.arange(24 * 1024, dtype=torch.int32, device="cuda").view(24, 1024)   # 4 KiB rows: bulk engine
+    want = x[r.src_of_dst.long()]
+    st = thd.new_status()
+    assert stall(torch.cuda.current_stream().cuda_stream) == L.OK
+    thd.swap(x, r, status=st)
+    assert thd.status_read(st) == L.ERR_TIMEOUT
+    thd.status_clear(st)
+    out = thd.swap(x, r, status=st)
+    assert thd.status_read(st) == L.OK
+    assert torch.equal(out, want)
 
 
 @pytest.mark.parametrize("width", [8, 128, 4096, 12288])

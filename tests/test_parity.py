@@ -454,6 +454,38 @@ def test_roll_labels_zigzag_parity(cp, depth):
         assert got[2].cpu().tolist() == want[2]
 
 
+@pytest.mark.parametrize("cp", [1, 4])
+def test_labels_and_partition_beyond_shared_memory(cp):
+    """13,000 documents (empty ones included): the label kernels and the
+    partition kernel search the boundaries in global memory instead of
+    shared memory.  Labels with MTP depth 2 and per-document extra tokens,
+    in both layouts, and the partition of every rank, against the oracle."""
+    rng = np.random.default_rng(123 + cp)
+    n = 13000
+    lp = [2 * cp * int(rng.integers(0, 4)) for _ in range(n)]
+    lv = [min(L, int(rng.integers(0, L + 3))) if L else 0 for L in lp]
+    cu_v, cu = _bounds(lv), _bounds(lp)
+    T = cu[-1]
+    tokens = [int(t) for t in rng.integers(0, 151936, size=T)]
+    nxt = [int(rng.integers(200000, 300000)) if (L and rng.random() < 0.3) else None for L in lv]
+    nt = torch.tensor([v or 0 for v in nxt], dtype=torch.int32, device="cuda")
+    hn = torch.tensor([int(v is not None) for v in nxt], dtype=torch.uint8, device="cuda")
+    tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+    st = thd.new_status()
+    got = thd.roll_labels(tok, _cu_tensor(cu_v), _cu_tensor(cu), 2, -5, status=st, next_token=nt, has_next=hn)
+    got_z = thd.roll_labels_zigzag(tok, _cu_tensor(cu_v), _cu_tensor(cu), cp, 2, -5, status=st, next_token=nt,
+                                   has_next=hn)
+    part = thd.partition_indices(_cu_tensor(cu), T, cp, -1, status=st)
+    one = thd.partition_indices(_cu_tensor(cu), T, cp, cp - 1, status=st)
+    thd.check_status(st)
+    want = oracle.roll_labels(tokens, cu_v, cu, 2, fill=-5, doc_next=nxt)
+    assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
+    want_z = oracle.roll_labels_zigzag(tokens, cu_v, cu, cp, 2, fill=-5, doc_next=nxt)
+    assert [g.cpu().tolist() for g in got_z] == [list(w) for w in want_z]
+    assert part.reshape(-1).cpu().tolist() == oracle.partition_indices(cu, T, cp, -1)
+    assert one.cpu().tolist() == oracle.partition_indices(cu, T, cp, cp - 1)
+
+
 def test_extra_tokens_pack_and_labels():
     """Rows with one extra token each: packing reports which documents it
     continues, and both label kernels take it as the target one past the
