@@ -20,7 +20,7 @@
 // quarter-warp that walk one token row reach eight different bank groups.
 // A block of 256 threads keeps a ring of three load buffers and two store
 // buffers; warp 0 issues every bulk copy (one lane per run).  Tiles of about
-// 24 KiB with three loads in flight per SM kept both directions at 0.89-0.96
+// 24 KiB with three loads in flight per SM kept both directions at 0.85-0.96
 // of the measured copy bandwidth on GB300 for pieces of 32 B - 768 B, against
 // 0.45-0.93 for the piece-by-piece engines.  Every wait is bounded: a wait that
 // runs out records THD_ERR_TIMEOUT, lets the block's copies in flight land and
