@@ -444,7 +444,8 @@ def run_thd(args, rank, world, local):
         piece = row_bytes // cp
         # the library's rule (copy.cu / ulysses_tile.cu): pieces that are
         # multiples of 16 bytes below 1 KiB take the tile transpose
-        engine = "ulysses_tile_kernel" if cp > 1 and piece % 16 == 0 and piece < 1024 else "row engine"
+        engine = ("tile transpose (ulysses_to_heads_kernel / ulysses_to_sequence_kernel)"
+                  if cp > 1 and piece % 16 == 0 and piece < 1024 else "row engine")
         uly = {"piece_bytes": piece, "engine": engine, "seq_to_head_us": round(to_head, 2),
                "head_to_seq_us": round(to_seq, 2),
                "gbs": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3, 1),

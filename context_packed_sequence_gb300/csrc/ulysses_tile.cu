@@ -6,36 +6,41 @@
 // head group; the head-sharded buffer holds, for each group h, every token's
 // piece h contiguously ([cp][T][P]).  Gathering pieces one by one (the row
 // engines in copy.cu) moves P bytes per copy, so small pieces leave HBM idle
-// between requests.  Here a tile of R consecutive tokens moves as a few large
-// bulk copies instead:
+// between requests.  Here a tile of R consecutive tokens (about 24 KiB) moves
+// as a few large bulk copies instead:
 //
-//   sequence -> head: one bulk load of the tile's R token rows (R*cp*P
-//     contiguous bytes), a shared-memory transpose into cp runs of R*P bytes,
-//     one bulk store per run to [h][g0 .. g0+R);
-//   head -> sequence: one bulk load per run, the transpose back, one bulk
-//     store of the R token rows.
+//   sequence -> head (ulysses_to_heads_kernel): one bulk load of the tile's R
+//     token rows (R*cp*P contiguous bytes), a shared-memory transpose into cp
+//     runs of R*P bytes, one bulk store per run to [h][g0 .. g0+R);
+//   head -> sequence (ulysses_to_sequence_kernel): one bulk load per run, the
+//     transpose back, one bulk store of the R token rows.
 //
 // The runs sit in shared memory at a padded stride of H16 16-byte units with
 // H16 = upr (mod 8), upr = P/16, so the eight 16-byte accesses of a
 // quarter-warp that walk one token row reach eight different bank groups.
-// A block of 256 threads keeps a ring of three load buffers and two store
-// buffers; warp 0 issues every bulk copy (one lane per run).  Tiles of about
-// 24 KiB with three loads in flight per SM kept both directions at 0.85-0.96
-// of the measured copy bandwidth on GB300 for pieces of 32 B - 768 B, against
-// 0.45-0.93 for the piece-by-piece engines.  Every wait is bounded: a wait that
-// runs out records THD_ERR_TIMEOUT, lets the block's copies in flight land and
-// returns.
+// Both kernels keep three load buffers and two store buffers per block, one
+// block per SM.  Sequence -> head runs as one block of 256 threads in step
+// (warp 0 issues the copies, one lane per run).  Head -> sequence, whose loads
+// are cp separate runs per tile, adds a warp that only loads: it refills a
+// buffer as soon as the eight transposing warps release it (an mbarrier with
+// eight arrivals), without waiting for their block barrier.  Measured on GB300
+// (of the copy bandwidth, pieces of 32 B - 768 B): sequence -> head 0.89-0.95,
+// head -> sequence 0.90-0.97 (0.85 for 32 B pieces with a block in step),
+// against 0.45-0.93 for the piece-by-piece engines.  Every wait is bounded: a
+// wait that runs out records THD_ERR_TIMEOUT, lets the block's copies in
+// flight land and returns.
 #include "thd_internal.cuh"
 #include "tma.cuh"
 
 namespace thd {
 namespace {
 
-constexpr int kTileThreads = 256;
 constexpr int kTileStages = 3;              // load buffers; two more for stores
 constexpr int64_t kTileTarget = 24 * 1024;  // bytes of token rows per tile
 constexpr int64_t kTileMaxPiece = 1024;     // larger pieces: the bulk row engine
 constexpr size_t kTileSmemLimit = 227 * 1024;
+constexpr int kTransposers = 256;                      // threads that transpose a tile
+constexpr int kToSequenceThreads = 32 + kTransposers;  // + the loading warp
 
 struct TileGeom {
   int32_t T, cp;
@@ -65,74 +70,86 @@ TileGeom tile_geom(int32_t T, int32_t cp, int64_t row_bytes) {
   return g;
 }
 
+// buffers, then one "loaded" and one "released" mbarrier per load buffer
 size_t tile_smem(const TileGeom& g) {
-  return static_cast<size_t>(kTileStages + 2) * g.stage + kTileStages * sizeof(uint64_t);
+  return static_cast<size_t>(kTileStages + 2) * g.stage + 2 * kTileStages * sizeof(uint64_t);
 }
 
+// The tiles of block b: tile b + i*G covers tokens [start(i), start(i) + rows(i)).
+struct TileSeq {
+  int32_t b, G, R, T;
+  __device__ __forceinline__ int64_t start(int i) const { return static_cast<int64_t>(b + i * G) * R; }
+  __device__ __forceinline__ int64_t rows(int i) const { return min(static_cast<int64_t>(R), T - start(i)); }
+};
+
+// Checked build: does every tile of this block lie inside [0, T)?  A block-
+// uniform answer; the default build compiles it to true.
+__device__ __forceinline__ bool tiles_in_range(const TileSeq& ts, int n_my, int32_t* status) {
+  if (!kChecked) return true;
+  bool bad = false;
+  if (threadIdx.x == 0)
+    for (int i = 0; i < n_my; ++i) bad |= !in_range(ts.start(i), 0, ts.T, status);
+  return !__syncthreads_or(bad);
+}
+
+// Unit k of a tile's token-major layout is (token ii, head h, unit v); its
+// place in the head-major runs is h*H16 + ii*upr + v.  Transposer `first` of
+// `stride` moves units first, first + stride, ...
 template <bool TO_HEAD>
-__global__ void __launch_bounds__(kTileThreads)
-ulysses_tile_kernel(const char* __restrict__ src, char* __restrict__ dst, TileGeom g, int32_t* status) {
+__device__ __forceinline__ void transpose_tile(const uint4* from, uint4* to, int rt, const TileGeom& g, int first,
+                                               int stride) {
+  const int units_per_row = g.cp * g.upr;
+  const int units = rt * units_per_row;
+#pragma unroll 4
+  for (int k = first; k < units; k += stride) {
+    const int ii = g.div_row.div(k);
+    const int rem = k - ii * units_per_row;
+    const int h = g.div_piece.div(rem);
+    const int run = h * g.H16 + ii * g.upr + (rem - h * g.upr);
+    if (TO_HEAD)
+      to[run] = from[k];
+    else
+      to[k] = from[run];
+  }
+}
+
+// ---- sequence -> head: one block of 256 threads in step ---------------------
+
+__global__ void __launch_bounds__(kTransposers)
+ulysses_to_heads_kernel(const char* __restrict__ src, char* __restrict__ dst, TileGeom g, int32_t* status) {
   extern __shared__ __align__(128) char smem[];
-  char* const loads = smem;                               // kTileStages buffers
-  char* const stores = smem + kTileStages * g.stage;      // 2 buffers
+  char* const loads = smem;                           // kTileStages buffers
+  char* const stores = smem + kTileStages * g.stage;  // 2 buffers
   uint64_t* const bars = reinterpret_cast<uint64_t*>(smem + (kTileStages + 2) * g.stage);
   const int tid = threadIdx.x, lane = tid & 31;
   const bool issuer = tid < 32;  // warp 0 issues the bulk copies
   pdl_wait_then_release();       // launched with programmatic dependent launch
   if (__syncthreads_or(tid == 0 && status_load(status) != 0)) return;
-  const int b = blockIdx.x, G = gridDim.x;
-  const int n_my = g.tiles > b ? (g.tiles - b + G - 1) / G : 0;
-  if (n_my == 0) return;
+  const TileSeq ts{static_cast<int32_t>(blockIdx.x), static_cast<int32_t>(gridDim.x), g.R, g.T};
+  const int n_my = g.tiles > ts.b ? (g.tiles - ts.b + ts.G - 1) / ts.G : 0;
+  if (n_my == 0 || !tiles_in_range(ts, n_my, status)) return;
   const int64_t P = static_cast<int64_t>(g.upr) * 16, row = P * g.cp;
-  const int units_per_row = g.cp * g.upr;
   if (tid == 0) {
     for (int s = 0; s < kTileStages; ++s) mbar_init(&bars[s], 1);
     mbar_init_fence();
   }
   __syncthreads();
 
-  // tile t covers tokens [t*R, t*R + rt)
-  auto tile_start = [&](int i) { return static_cast<int64_t>(b + i * G) * g.R; };
-  auto tile_rows = [&](int64_t g0) { return min(static_cast<int64_t>(g.R), g.T - g0); };
-  // checked build: every tile of this block lies inside [0, T), else the
-  // block moves nothing (no bulk copy has been issued yet)
-  if (kChecked) {
-    bool bad = false;
-    if (tid == 0)
-      for (int i = 0; i < n_my; ++i) bad |= !in_range(tile_start(i), 0, g.T, status);
-    if (__syncthreads_or(bad)) return;
-  }
-
-  // warp 0 only: lane 0 arms the stage's barrier before any lane loads into it
+  // warp 0 only: lane 0 loads the tile's token rows in one copy
   auto issue_load = [&](int i) {
     const int s = i % kTileStages;
-    const int64_t g0 = tile_start(i), rt = tile_rows(g0);
-    char* buf = loads + s * g.stage;
-    if (TO_HEAD) {
-      if (lane == 0) {
-        const uint32_t bytes = static_cast<uint32_t>(rt * row);
-        mbar_arrive_expect_tx(&bars[s], bytes);
-        bulk_load(buf, src + g0 * row, bytes, &bars[s]);
-      }
-    } else {
-      const uint32_t bytes = static_cast<uint32_t>(rt * P);
-      if (lane == 0) mbar_arrive_expect_tx(&bars[s], bytes * static_cast<uint32_t>(g.cp));
-      __syncwarp();
-      for (int h = lane; h < g.cp; h += 32)
-        bulk_load(buf + static_cast<int64_t>(h) * g.H16 * 16, src + (static_cast<int64_t>(h) * g.T + g0) * P,
-                  bytes, &bars[s]);
+    if (lane == 0) {
+      const uint32_t bytes = static_cast<uint32_t>(ts.rows(i) * row);
+      mbar_arrive_expect_tx(&bars[s], bytes);
+      bulk_load(loads + s * g.stage, src + ts.start(i) * row, bytes, &bars[s]);
     }
   };
+  // warp 0 only: one lane per head-group run
   auto issue_store = [&](int i) {
-    const int64_t g0 = tile_start(i), rt = tile_rows(g0);
     const char* buf = stores + (i & 1) * g.stage;
-    if (TO_HEAD) {
-      for (int h = lane; h < g.cp; h += 32)
-        bulk_store(dst + (static_cast<int64_t>(h) * g.T + g0) * P, buf + static_cast<int64_t>(h) * g.H16 * 16,
-                   static_cast<uint32_t>(rt * P));
-    } else if (lane == 0) {
-      bulk_store(dst + g0 * row, buf, static_cast<uint32_t>(rt * row));
-    }
+    for (int h = lane; h < g.cp; h += 32)
+      bulk_store(dst + (static_cast<int64_t>(h) * g.T + ts.start(i)) * P, buf + static_cast<int64_t>(h) * g.H16 * 16,
+                 static_cast<uint32_t>(ts.rows(i) * P));
     bulk_commit();
   };
 
@@ -150,23 +167,9 @@ ulysses_tile_kernel(const char* __restrict__ src, char* __restrict__ dst, TileGe
       timed_out = true;
       break;
     }
-    // unit k of the token-major layout is (token ii, head h, unit v); its
-    // place in the head-major runs is h*H16 + ii*upr + v
-    const int rt = static_cast<int>(tile_rows(tile_start(i)));
-    const uint4* from = reinterpret_cast<const uint4*>(loads + s * g.stage);
-    uint4* to = reinterpret_cast<uint4*>(stores + (i & 1) * g.stage);
-    const int units = rt * units_per_row;
-#pragma unroll 4
-    for (int k = tid; k < units; k += kTileThreads) {
-      const int ii = g.div_row.div(k);
-      const int rem = k - ii * units_per_row;
-      const int h = g.div_piece.div(rem);
-      const int run = h * g.H16 + ii * g.upr + (rem - h * g.upr);
-      if (TO_HEAD)
-        to[run] = from[k];
-      else
-        to[k] = from[run];
-    }
+    transpose_tile<true>(reinterpret_cast<const uint4*>(loads + s * g.stage),
+                         reinterpret_cast<uint4*>(stores + (i & 1) * g.stage), static_cast<int>(ts.rows(i)), g, tid,
+                         kTransposers);
     fence_proxy_async_shared();  // the bulk stores read what this thread wrote
     __syncthreads();             // ... and load buffer s is free again
     if (issuer) {
@@ -186,18 +189,112 @@ ulysses_tile_kernel(const char* __restrict__ src, char* __restrict__ dst, TileGe
   if (issuer) bulk_wait_all();
 }
 
-template <bool TO_HEAD>
-thd_status_t launch_tiles(const void* src, void* dst, const TileGeom& g, size_t smem, int32_t* status,
-                          cudaStream_t s) {
-  auto kernel = ulysses_tile_kernel<TO_HEAD>;
+// ---- head -> sequence: a loading warp and eight transposing warps -----------
+
+// the transposing threads (warps 1-8) among themselves: named barriers 1 and 2
+__device__ __forceinline__ void transposers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kTransposers) : "memory");
+}
+__device__ __forceinline__ bool transposers_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 2, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kTransposers)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(kToSequenceThreads)
+ulysses_to_sequence_kernel(const char* __restrict__ src, char* __restrict__ dst, TileGeom g, int32_t* status) {
+  extern __shared__ __align__(128) char smem[];
+  char* const loads = smem;                           // kTileStages buffers
+  char* const stores = smem + kTileStages * g.stage;  // 2 buffers
+  uint64_t* const loaded = reinterpret_cast<uint64_t*>(smem + (kTileStages + 2) * g.stage);
+  uint64_t* const released = loaded + kTileStages;    // 8 arrivals: every transposing warp is done
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait_then_release();  // launched with programmatic dependent launch
+  if (__syncthreads_or(tid == 0 && status_load(status) != 0)) return;
+  const TileSeq ts{static_cast<int32_t>(blockIdx.x), static_cast<int32_t>(gridDim.x), g.R, g.T};
+  const int n_my = g.tiles > ts.b ? (g.tiles - ts.b + ts.G - 1) / ts.G : 0;
+  if (n_my == 0 || !tiles_in_range(ts, n_my, status)) return;
+  const int64_t P = static_cast<int64_t>(g.upr) * 16, row = P * g.cp;
+  if (tid == 0) {
+    for (int s = 0; s < kTileStages; ++s) {
+      mbar_init(&loaded[s], 1);
+      mbar_init(&released[s], kTransposers / 32);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // the loading warp: tile i goes into buffer i % stages once the tile
+    // before it there is released; one lane per head-group run
+    int issued = 0;
+    for (int i = 0; i < n_my; ++i) {
+      const int s = i % kTileStages;
+      if (i >= kTileStages &&
+          !__all_sync(kFullMask, mbar_wait(&released[s], static_cast<uint32_t>((i / kTileStages - 1) & 1))))
+        break;  // the transposing warps gave up; they report it
+      const uint32_t bytes = static_cast<uint32_t>(ts.rows(i) * P);
+      if (lane == 0) mbar_arrive_expect_tx(&loaded[s], bytes * static_cast<uint32_t>(g.cp));
+      __syncwarp();
+      char* buf = loads + s * g.stage;
+      for (int h = lane; h < g.cp; h += 32)
+        bulk_load(buf + static_cast<int64_t>(h) * g.H16 * 16, src + (static_cast<int64_t>(h) * g.T + ts.start(i)) * P,
+                  bytes, &loaded[s]);
+      issued = i + 1;
+    }
+    // every load this warp issued lands before it leaves (each buffer has at
+    // most its last phase open, so these waits end)
+    if (lane == 0)
+      for (int j = max(0, issued - kTileStages); j < issued; ++j)
+        mbar_wait(&loaded[j % kTileStages], static_cast<uint32_t>((j / kTileStages) & 1));
+    return;
+  }
+
+  // the transposing warps; warp 1 also stores
+  const bool storer = warp == 1;
+  bool timed_out = false;
+  for (int i = 0; i < n_my; ++i) {
+    const int s = i % kTileStages;
+    if (storer) bulk_wait_read_all_but_one();  // the store of tile i-2 is done reading buffer i & 1
+    transposers_sync();
+    if (!transposers_all(mbar_wait(&loaded[s], static_cast<uint32_t>((i / kTileStages) & 1)))) {
+      timed_out = true;  // give up together
+      break;
+    }
+    transpose_tile<false>(reinterpret_cast<const uint4*>(loads + s * g.stage),
+                          reinterpret_cast<uint4*>(stores + (i & 1) * g.stage), static_cast<int>(ts.rows(i)), g,
+                          tid - 32, kTransposers);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&released[s]);  // this warp is done reading buffer s
+    fence_proxy_async_shared();                // the bulk store reads what this thread wrote
+    transposers_sync();
+    if (storer && lane == 0) {
+      bulk_store(dst + ts.start(i) * row, stores + (i & 1) * g.stage, static_cast<uint32_t>(ts.rows(i) * row));
+      bulk_commit();
+    }
+  }
+  if (timed_out && tid == 32) status_set(status, THD_ERR_TIMEOUT);
+  if (storer) bulk_wait_all();
+}
+
+template <class Kernel>
+thd_status_t launch_tiles(Kernel kernel, int threads, const void* src, void* dst, const TileGeom& g, size_t smem,
+                          int32_t* status, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   int per_sm = 0;
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kTileThreads, smem);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
   if (e == cudaSuccess) {
     if (per_sm < 1) per_sm = 1;
     int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
     if (grid > g.tiles) grid = g.tiles;
-    e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), kTileThreads, smem, s, static_cast<const char*>(src),
+    e = launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), threads, smem, s, static_cast<const char*>(src),
                    static_cast<char*>(dst), g, status);
   }
   if (e != cudaSuccess) {
@@ -221,8 +318,8 @@ thd_status_t launch_ulysses_tiles(const void* src, void* dst, int32_t T, int32_t
                                   bool seq_to_head, int32_t* status, cudaStream_t s) {
   const TileGeom g = tile_geom(T, cp, row_bytes);
   const size_t smem = tile_smem(g);
-  return seq_to_head ? launch_tiles<true>(src, dst, g, smem, status, s)
-                     : launch_tiles<false>(src, dst, g, smem, status, s);
+  return seq_to_head ? launch_tiles(ulysses_to_heads_kernel, kTransposers, src, dst, g, smem, status, s)
+                     : launch_tiles(ulysses_to_sequence_kernel, kToSequenceThreads, src, dst, g, smem, status, s);
 }
 
 }  // namespace thd
