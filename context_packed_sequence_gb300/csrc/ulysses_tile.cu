@@ -24,9 +24,10 @@
 // are cp separate runs per tile, adds a warp that only loads: it refills a
 // buffer as soon as the eight transposing warps release it (an mbarrier with
 // eight arrivals), without waiting for their block barrier.  Measured on GB300
-// (of the copy bandwidth, pieces of 32 B - 768 B): sequence -> head 0.89-0.95,
-// head -> sequence 0.90-0.97 (0.85 for 32 B pieces with a block in step),
-// against 0.45-0.93 for the piece-by-piece engines.  Every wait is bounded: a
+// (of the copy bandwidth, pieces of 32 B - 768 B, 0.5 GiB buffers): sequence ->
+// head 0.89-0.95, head -> sequence 0.90-0.97 (0.85 for 32 B pieces with a
+// block in step), against 0.45-0.93 for the piece-by-piece engines; 1 GiB
+// buffers of 16-128 B pieces: 0.97-0.995.  Every wait is bounded: a
 // wait that runs out records THD_ERR_TIMEOUT, lets the block's copies in
 // flight land and returns.
 #include "thd_internal.cuh"
