@@ -159,6 +159,20 @@ def plan_kernel_name(row_bytes: int) -> str:
     return f"bulk_copy_kernel<{nst}, SwapMap, false> (thd_swap)"
 
 
+def smi_gpu_id(device) -> str:
+    """The nvidia-smi id of a CUDA device: its PCI address, which does not
+    depend on CUDA_VISIBLE_DEVICES; else its index mapped through that list."""
+    try:
+        p = torch.cuda.get_device_properties(device)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except (AttributeError, RuntimeError, AssertionError):
+        pass
+    ids = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    if device.index is not None and device.index < len(ids):
+        return ids[device.index]
+    return str(device.index or 0)
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -166,8 +180,8 @@ class ClockSampler:
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
         self.proc = None
         self.out = None
 
@@ -175,7 +189,7 @@ class ClockSampler:
         try:
             self.out = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
@@ -307,7 +321,7 @@ def run_thd(args, rank, world, local):
     n_ev = args.steps
     ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev + 1)]
     ev_sw = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
-    clocks = ClockSampler(device.index).start() if rank == 0 else None
+    clocks = ClockSampler(smi_gpu_id(device)).start() if rank == 0 else None
     barrier(world, device)
     torch.cuda.synchronize(device)
     ev_step[0].record(stream)

@@ -44,3 +44,23 @@ def test_gpu_arm_contract():
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["swap_us_distribution"]["p10"] <= d["swap_us_distribution"]["p90"]
+
+
+def test_clock_sampler_targets_the_benchmarked_gpu(monkeypatch):
+    """nvidia-smi is asked about the GPU the benchmark runs on: its PCI
+    address when torch reports one, else the index through CUDA_VISIBLE_DEVICES."""
+    import types
+    import torch
+    import bench
+    dev = torch.device("cuda", 1)
+    props = types.SimpleNamespace(pci_domain_id=0, pci_bus_id=0x1B, pci_device_id=0)
+    monkeypatch.setattr(torch.cuda, "get_device_properties", lambda d: props)
+    assert bench.smi_gpu_id(dev) == "00000000:1B:00.0"
+
+    def no_props(d):
+        raise AttributeError("no pci fields")
+    monkeypatch.setattr(torch.cuda, "get_device_properties", no_props)
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3,5")
+    assert bench.smi_gpu_id(dev) == "5"
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
+    assert bench.smi_gpu_id(dev) == "1"
