@@ -514,7 +514,7 @@ def run_thd(args, rank, world, local):
             "traffic": traffic if w.name == "lognorm128k" else None,
             "algorithmic_bytes_per_launch": swap_bytes,
         },
-        "gpu_launches": launches_per_step * n_ev,
+        "gpu_launches": launches_per_step * n_ev * world,   # every rank's, like value
         "clocks": clock_rec,
     }
     if e2e is not None:
