@@ -526,55 +526,58 @@ def run_thd(args, rank, world, local):
     return result, dict(x=x, T=T, cu=cu_d, w=w, row_bytes=row_bytes)
 
 
-def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes, steps=12):
+def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes, steps=12, slots=3):
     """End to end through the public API with host buffers.  Every step copies
     its input (x and the boundaries) from pinned host memory to the device,
     builds both routes, runs the layers' swap pairs and copies the result back
-    to pinned host memory.  Uploads and downloads run on a copy stream, double
-    buffered, so step i+1's upload and step i's download overlap step i+1's
-    and step i+2's compute; the timed region spans the first upload to the
-    last download."""
+    to pinned host memory.  Uploads and downloads run on two copy streams of
+    their own over `slots` device buffers, so uploads, downloads (the link is
+    full duplex) and compute overlap; a slot is uploaded again only once its
+    previous result has been read back.  The timed region spans the first
+    upload to the last download."""
     x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_host.copy_(x)
     cu_host = cu_d.cpu().pin_memory()
-    out_host = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
-    xd = [torch.empty_like(x) for _ in range(2)]
-    yd = [torch.empty_like(x) for _ in range(2)]
-    cud = [torch.empty_like(cu_d) for _ in range(2)]
+    out_host = [torch.empty_like(x_host).pin_memory() for _ in range(slots)]
+    xd = [torch.empty_like(x) for _ in range(slots)]
+    yd = [torch.empty_like(x) for _ in range(slots)]
+    cud = [torch.empty_like(cu_d) for _ in range(slots)]
     st = thd.new_status(device)
     routes = (thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device), thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device))
     ks = torch.cuda.current_stream(device)
-    cs = torch.cuda.Stream(device)
+    ups, downs = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    cs = ups  # the link-only timings below
 
     def run(n):
         up = [torch.cuda.Event() for _ in range(n)]
         done = [torch.cuda.Event() for _ in range(n)]
-        down = torch.cuda.Event()
+        freed = [torch.cuda.Event() for _ in range(n)]
 
         def upload(i):
-            with torch.cuda.stream(cs):
-                xd[i % 2].copy_(x_host, non_blocking=True)
-                cud[i % 2].copy_(cu_host, non_blocking=True)
-                up[i].record(cs)
+            with torch.cuda.stream(ups):
+                if i >= slots:
+                    ups.wait_event(freed[i - slots])  # the slot's last result is read back
+                xd[i % slots].copy_(x_host, non_blocking=True)
+                cud[i % slots].copy_(cu_host, non_blocking=True)
+                up[i].record(ups)
 
-        upload(0)
-        if n > 1:
-            upload(1)
+        for i in range(min(slots, n)):
+            upload(i)
         for i in range(n):
-            k = i % 2
+            k = i % slots
             ks.wait_event(up[i])
             fwd, bwd = thd.route_build_pair(cud[k], T, cp, status=st, routes=routes, stream=ks)
             for _ in range(layers):
                 thd.swap(xd[k], fwd, out=yd[k], status=st, stream=ks)
                 thd.swap(yd[k], bwd, out=xd[k], status=st, stream=ks)
             done[i].record(ks)
-            with torch.cuda.stream(cs):
-                cs.wait_event(done[i])
+            with torch.cuda.stream(downs):
+                downs.wait_event(done[i])
                 out_host[k].copy_(xd[k], non_blocking=True)
-                if i + 2 < n:
-                    upload(i + 2)
-        down.record(cs)
-        ks.wait_event(down)
+                freed[i].record(downs)
+            if i + slots < n:
+                upload(i + slots)
+        ks.wait_stream(downs)
 
     run(2)
     torch.cuda.synchronize(device)
@@ -594,7 +597,8 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
     barrier(world, device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(ks)
-    cs.wait_stream(ks)
+    ups.wait_stream(ks)
+    downs.wait_stream(ks)
     run(steps)
     e1.record(ks)
     torch.cuda.synchronize(device)
@@ -607,7 +611,7 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
             "h2d_bytes_per_step": int(x.numel() * x.element_size() + cu_d.numel() * 4),
             "d2h_bytes_per_step": int(x.numel() * x.element_size()),
             "ms_per_step": round(ms / steps, 3), "steps": steps,
-            "overlap": "uploads/downloads on a copy stream, double buffered against compute",
+            "overlap": f"uploads and downloads on two copy streams, {slots} buffer slots, against compute",
             "link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
