@@ -32,6 +32,7 @@
 // flight land and returns.
 #include "thd_internal.cuh"
 #include "tma.cuh"
+#include "thd_debug.h"
 
 namespace thd {
 namespace {
@@ -42,6 +43,15 @@ constexpr int64_t kTileMaxPiece = 1024;     // larger pieces: the bulk row engin
 constexpr size_t kTileSmemLimit = 227 * 1024;
 constexpr int kTransposers = 256;                      // threads that transpose a tile
 constexpr int kToSequenceThreads = 32 + kTransposers;  // + the loading warp
+
+// Checked build only: a one-shot request (thd_debug_stall_next_ulysses_tile)
+// that block 0 of the next tile kernel arms 16 bytes no copy delivers on its
+// first buffer, so the timeout path runs for real.
+__device__ int g_tile_stall_request;
+
+__device__ __forceinline__ void maybe_stall(int i, uint64_t* bar) {
+  if (kChecked && i == 0 && blockIdx.x == 0 && atomicExch(&g_tile_stall_request, 0) != 0) mbar_expect_tx(bar, 16);
+}
 
 struct TileGeom {
   int32_t T, cp;
@@ -142,6 +152,7 @@ ulysses_to_heads_kernel(const char* __restrict__ src, char* __restrict__ dst, Ti
     if (lane == 0) {
       const uint32_t bytes = static_cast<uint32_t>(ts.rows(i) * row);
       mbar_arrive_expect_tx(&bars[s], bytes);
+      maybe_stall(i, &bars[s]);
       bulk_load(loads + s * g.stage, src + ts.start(i) * row, bytes, &bars[s]);
     }
   };
@@ -242,7 +253,10 @@ ulysses_to_sequence_kernel(const char* __restrict__ src, char* __restrict__ dst,
           !__all_sync(kFullMask, mbar_wait(&released[s], static_cast<uint32_t>((i / kTileStages - 1) & 1))))
         break;  // the transposing warps gave up; they report it
       const uint32_t bytes = static_cast<uint32_t>(ts.rows(i) * P);
-      if (lane == 0) mbar_arrive_expect_tx(&loaded[s], bytes * static_cast<uint32_t>(g.cp));
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&loaded[s], bytes * static_cast<uint32_t>(g.cp));
+        maybe_stall(i, &loaded[s]);
+      }
       __syncwarp();
       char* buf = loads + s * g.stage;
       for (int h = lane; h < g.cp; h += 32)
@@ -324,3 +338,17 @@ thd_status_t launch_ulysses_tiles(const void* src, void* dst, int32_t T, int32_t
 }
 
 }  // namespace thd
+
+#if defined(THD_CHECKED) && THD_CHECKED
+// Declared in include/thd_debug.h; exported by the checked build only.
+extern "C" thd_status_t thd_debug_stall_next_ulysses_tile(cudaStream_t stream) {
+  const int one = 1;
+  const cudaError_t e =
+      cudaMemcpyToSymbolAsync(thd::g_tile_stall_request, &one, sizeof(one), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) {
+    thd::record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  return THD_OK;
+}
+#endif

@@ -25,6 +25,15 @@ extern "C" {
  */
 thd_status_t thd_debug_stall_next_bulk_copy(cudaStream_t stream);
 
+/*
+ * The same one-shot request for the Ulysses tile transpose (thd_ulysses_swap
+ * with head-group pieces of 16 B - 1008 B in steps of 16): block 0 of the
+ * next tile kernel waits on its first buffer for 16 bytes that never come;
+ * its waits give up (about 3 s each), the block lets its other copies land,
+ * records THD_ERR_TIMEOUT and returns.
+ */
+thd_status_t thd_debug_stall_next_ulysses_tile(cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -197,6 +197,29 @@ def test_bulk_wait_that_runs_out_reports_timeout():
     assert torch.equal(out, want)
 
 
+@pytest.mark.skipif(os.environ.get("THD_CHECKED") != "1", reason="the debug request is in the checked build only")
+@pytest.mark.parametrize("direction", [thd.SEQ_TO_HEAD, thd.HEAD_TO_SEQ])
+def test_ulysses_tile_wait_that_runs_out_reports_timeout(direction):
+    """Block 0 of the tile transpose waits on its first buffer for 16 bytes
+    that never come: sequence -> head gives up as one block, head -> sequence
+    through its loading warp and transposing warps; either way the status
+    says THD_ERR_TIMEOUT and the next exchange on the same context is exact."""
+    lib = L.load()
+    stall = lib.thd_debug_stall_next_ulysses_tile
+    stall.restype, stall.argtypes = ctypes.c_int, [ctypes.c_void_p]
+    cp, T = 16, 4096
+    x = torch.randint(0, 256, (T, cp, 32), dtype=torch.uint8, device="cuda")     # 32-byte head groups
+    src = x if direction == thd.SEQ_TO_HEAD else thd.ulysses_swap(x, cp, thd.SEQ_TO_HEAD)
+    want = thd.ulysses_swap(src, cp, direction)
+    st = thd.new_status()
+    assert stall(torch.cuda.current_stream().cuda_stream) == L.OK
+    thd.ulysses_swap(src, cp, direction, status=st)
+    assert thd.status_read(st) == L.ERR_TIMEOUT
+    thd.status_clear(st)
+    assert torch.equal(thd.ulysses_swap(src, cp, direction, status=st), want)
+    assert thd.status_read(st) == L.OK
+
+
 @pytest.mark.parametrize("width", [8, 128, 4096, 12288])
 def test_corrupted_route_index_is_range_checked(width):
     """An out-of-range entry is skipped by the kernel's own check (the access
