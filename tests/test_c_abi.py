@@ -47,3 +47,29 @@ def test_c_program_runs(tmp_path):
     exe = _compile(tmp_path)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
+
+
+def test_debug_header_links_against_the_checked_build(tmp_path):
+    """include/thd_debug.h is plain C too, and its entry points resolve in
+    libthd_checked.so (the default library does not export them)."""
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    checked = os.path.join(PKG, "libthd_checked.so")
+    if not os.path.exists(checked):
+        from context_packed_sequence_gb300 import build
+        build.build(checked=True)
+    src = tmp_path / "debug.c"
+    src.write_text('#include "thd_debug.h"\n'
+                   "int main(void) {\n"
+                   "  thd_status_t (*a)(cudaStream_t) = thd_debug_stall_next_bulk_copy;\n"
+                   "  thd_status_t (*b)(cudaStream_t) = thd_debug_stall_next_ulysses_tile;\n"
+                   "  return (a != 0 && b != 0) ? 0 : 1;\n"
+                   "}\n")
+    exe = str(tmp_path / "debug")
+    cmd = [cc, "-std=c11", "-Wall", "-Werror", "-O2", str(src), "-o", exe,
+           "-I", os.path.join(ROOT, "include"), "-I", os.path.join(CUDA, "include"),
+           "-L", PKG, "-l:libthd_checked.so", f"-Wl,-rpath,{PKG}",
+           "-L", _cuda_lib_dir(), "-lcudart", f"-Wl,-rpath,{_cuda_lib_dir()}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
