@@ -188,6 +188,25 @@ def _check_invariants(cu, T, cp):
     assert bwd == sum(zz, [])
 
 
+def test_random_packings_keep_every_invariant():
+    """Beyond the exhaustive small cases: packings of up to 24 documents
+    (empty ones included) for cp = 1 .. 16, drawn by hypothesis
+    (deterministically), satisfy every invariant above and agree with the
+    interval-intersection reading in both directions."""
+    pytest.importorskip("hypothesis")
+    from hypothesis import given, settings, strategies as st
+
+    @settings(max_examples=150, deadline=None, derandomize=True)
+    @given(cp=st.integers(1, 16), units=st.lists(st.integers(0, 6), max_size=24))
+    def check(cp, units):
+        cu = [0]
+        for u in units:
+            cu.append(cu[-1] + 2 * cp * u)
+        _check_invariants(cu, cu[-1], cp)
+
+    check()
+
+
 @pytest.mark.parametrize("cp", [1, 2, 3, 4])
 def test_bruteforce_small_packings(cp):
     n = 0
