@@ -255,6 +255,33 @@ def test_ulysses_parity(cp, T, heads, head_bytes):
     assert torch.equal(back, x)
 
 
+def test_ulysses_fuzz():
+    """40 random shapes through every engine of the exchange: cp 1-16, pieces
+    of 1-1040 bytes (multiples of 16 below 1 KiB take the tile transpose,
+    larger or odd ones the row engines), token counts that leave ragged last
+    tiles; both directions against the oracle."""
+    rng = np.random.default_rng(2027)
+    engines = set()
+    for case in range(40):
+        cp = int(rng.integers(1, 17))
+        if case % 2:
+            piece = 16 * int(rng.integers(1, 66))         # 16 .. 1040, mostly the tile transpose
+        else:
+            piece = int(rng.integers(1, 300))             # odd sizes: the 16/4/1-byte unit engine
+        T = cp * int(rng.integers(1, max(2, 200000 // (cp * cp * piece + 1))))
+        engines.add("tile" if cp > 1 and piece % 16 == 0 and piece < 1024 else "rows")
+        x_np = rng.integers(0, 256, size=(T, cp * piece), dtype=np.uint8)
+        want = oracle.ulysses_swap(x_np, cp, oracle.SEQ_TO_HEAD)
+        x = torch.from_numpy(x_np).cuda().view(T, cp, piece)
+        st = thd.new_status()
+        y = thd.ulysses_swap(x, cp, thd.SEQ_TO_HEAD, status=st)
+        back = thd.ulysses_swap(y, cp, thd.HEAD_TO_SEQ, status=st)
+        thd.check_status(st)
+        assert np.array_equal(y.cpu().numpy().reshape(cp * T, piece), want), (cp, T, piece)
+        assert torch.equal(back, x), (cp, T, piece)
+    assert engines == {"tile", "rows"}
+
+
 @pytest.mark.parametrize("cp,T,piece", [(16, 19984, 32), (3, 1503, 48), (8, 424, 512)])
 def test_ulysses_guard_bytes_untouched(cp, T, piece):
     """The tile transpose writes exactly its output: 256 guard bytes on each
