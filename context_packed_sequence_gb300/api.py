@@ -194,6 +194,9 @@ def partition_indices(cu_seqlens_padded: torch.Tensor, T: int, cp: int, rank: in
     shape = (cp, S) if rank == -1 else (S,)
     if out is None:
         out = torch.empty(shape, dtype=torch.int32, device=cu_seqlens_padded.device)
+    _need_cuda(out, "out", torch.int32)
+    if out.numel() != (cp * S if rank == -1 else S):
+        raise ValueError(f"out must hold {shape} int32, got shape {tuple(out.shape)}")
     if status is None:
         status = new_status(cu_seqlens_padded.device)
     code = L.load().thd_partition_indices(_ptr(cu_seqlens_padded), cu_seqlens_padded.numel() - 1, int(T),
@@ -206,11 +209,16 @@ def _copy(fn_name, x, route, out, status, stream):
     _need_cuda(x, "x")
     if x.dim() < 1 or x.shape[0] != route.T:
         raise ValueError(f"x must have {route.T} rows, got shape {tuple(x.shape)}")
+    if x.device != route.device:
+        raise ValueError(f"x is on {x.device}, the route on {route.device}")
     if out is None:
         out = torch.empty_like(x)
     _need_cuda(out, "out")
-    if out.shape != x.shape or out.dtype != x.dtype:
-        raise ValueError("out must match x in shape and dtype")
+    if out.shape != x.shape or out.dtype != x.dtype or out.device != x.device:
+        raise ValueError("out must match x in shape, dtype and device")
+    if status is None:
+        # the route's own status word: a route whose build failed moves nothing
+        status = getattr(route, "status", None)
     row_bytes = (x[0].numel() if x.shape[0] else 1) * x.element_size()
     if x.numel() == 0:
         return out
@@ -222,7 +230,10 @@ def _copy(fn_name, x, route, out, status, stream):
 
 
 def swap(x, route: Route, out=None, status=None, stream=None):
-    """Fused layout swap: out[q] = x[route.src_of_dst[q]] (rows = x's first dim)."""
+    """Fused layout swap: out[q] = x[route.src_of_dst[q]] (rows = x's first dim).
+
+    status defaults to the route's status word (set by its build), so a swap
+    through a route whose build failed writes nothing."""
     return _copy("thd_swap", x, route, out, status, stream)
 
 

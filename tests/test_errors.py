@@ -78,6 +78,27 @@ def test_host_errors_raise_at_once():
     assert e.value.kind == "invalid_arg"
 
 
+def test_binding_checks_outputs_and_follows_the_route_status():
+    """partition_indices refuses an output of the wrong size; a swap given no
+    status word uses the route's, so a route whose build failed moves nothing."""
+    cu = torch.tensor([0, 8, 16], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        thd.partition_indices(cu, 16, 2, -1, out=torch.empty(15, dtype=torch.int32, device="cuda"))
+    with pytest.raises(TypeError):
+        thd.partition_indices(cu, 16, 2, 0, out=torch.empty(8, dtype=torch.int64, device="cuda"))
+    got = thd.partition_indices(cu, 16, 2, 0, out=torch.empty(8, dtype=torch.int32, device="cuda"))
+    assert got.tolist() == oracle.partition_indices([0, 8, 16], 16, 2, 0)
+
+    bad = thd.route_build(torch.tensor([0, 6, 16], dtype=torch.int32, device="cuda"), 16, 2, Z2C)
+    x = torch.arange(16 * 8, dtype=torch.int32, device="cuda").view(16, 8)
+    out = torch.full_like(x, -7)
+    thd.swap(x, bad, out=out)
+    assert thd.status_read(bad.status) == L.ERR_LEN_NOT_DIVISIBLE
+    assert bool((out == -7).all())
+    good = thd.route_build(cu, 16, 2, Z2C)
+    assert torch.equal(thd.swap(x, good), x[good.src_of_dst.long()])
+
+
 def test_pair_refuses_swapped_directions():
     cu = torch.tensor([0, 8], dtype=torch.int32, device="cuda")
     fwd, bwd = thd.Route(8, 2, Z2C), thd.Route(8, 2, C2Z)
