@@ -37,6 +37,56 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
     assert sorted(L.SIGNATURES) == names
 
 
+def _declarations():
+    """(name, return type, [parameter types]) of every function in thd.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = []
+    for m in re.finditer(r"([A-Za-z_][\w \*]*?)\b(thd_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        types = []
+        if params and params != "void":
+            for p in params.split(","):
+                p = " ".join(p.split())
+                types.append(re.sub(r"\s*\b[A-Za-z_]\w*$", "", p) if not p.endswith("*") else p)
+        out.append((name, ret, types))
+    return out
+
+
+def _ctype_for(c_type, is_return=False):
+    import ctypes as C
+    t = " ".join(c_type.replace("*", " * ").split())
+    if t.endswith("*"):
+        base = t[:-1].replace("const", "").strip()
+        if base == "thd_route_t":
+            return ("pointer", "ThdRoute")
+        if base == "char":
+            return C.c_char_p
+        if base == "int32_t" and not is_return:
+            return ("pointer", "c_int32_or_void")
+        return C.c_void_p
+    base = t.replace("const", "").strip()
+    return {"int64_t": C.c_int64, "int32_t": C.c_int32, "size_t": C.c_size_t, "thd_status_t": C.c_int32,
+            "thd_dir_t": C.c_int32, "thd_ulysses_dir_t": C.c_int32, "cudaStream_t": C.c_void_p}[base]
+
+
+def test_ctypes_signatures_match_the_header_parameter_by_parameter():
+    import ctypes as C
+    decls = _declarations()
+    assert sorted(d[0] for d in decls) == sorted(L.SIGNATURES)
+    for name, ret, params in decls:
+        res, args = L.SIGNATURES[name]
+        assert res is _ctype_for(ret, is_return=True), (name, ret, res)
+        assert len(args) == len(params), (name, params, args)
+        for i, (p, a) in enumerate(zip(params, args)):
+            want = _ctype_for(p)
+            if want == ("pointer", "ThdRoute"):
+                assert a is C.POINTER(L.ThdRoute), (name, i, p, a)
+            elif want == ("pointer", "c_int32_or_void"):
+                assert a in (C.c_void_p, C.POINTER(C.c_int32)), (name, i, p, a)
+            else:
+                assert a is want, (name, i, p, a)
+
+
 def test_status_codes_match_header(lib):
     text = open(HEADER).read()
     codes = dict((k, int(v)) for k, v in re.findall(r"THD_(OK|ERR_[A-Z_]+)\s*=\s*(\d+)", text))
