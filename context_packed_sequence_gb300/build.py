@@ -51,14 +51,18 @@ def _compile(args):
     return src, cmd, r
 
 
-def build(extra_flags=(), verbose: bool = False, checked: bool = False) -> str:
+def _variant(checked: bool, extra_flags=()):
     build_dir, lib_path = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
     flags = list(extra_flags) + (["-DTHD_CHECKED=1"] if checked else [])
     os.makedirs(build_dir, exist_ok=True)
-    jobs = []
-    for src in sources():
-        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
-        jobs.append((src, obj, flags))
+    jobs = [(src, os.path.join(build_dir, os.path.basename(src)[:-3] + ".o"), flags) for src in sources()]
+    return lib_path, jobs
+
+
+def _build(variants, verbose: bool = False) -> list:
+    """Compile every variant's translation units in one parallel pool, then
+    link each library."""
+    jobs = [j for _, js in variants for j in js]
     with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
         results = list(ex.map(_compile, jobs))
     failed = False
@@ -68,14 +72,25 @@ def build(extra_flags=(), verbose: bool = False, checked: bool = False) -> str:
         failed |= r.returncode != 0
     if failed:
         raise RuntimeError("libthd: compilation failed (see the nvcc output above)")
-    tmp = lib_path + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[j[1] for j in jobs]]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
-        raise RuntimeError("libthd: link failed")
-    os.replace(tmp, lib_path)
-    return lib_path
+    for lib_path, js in variants:
+        tmp = lib_path + ".tmp"
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[j[1] for j in js]]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+            raise RuntimeError("libthd: link failed")
+        os.replace(tmp, lib_path)
+    return [lib_path for lib_path, _ in variants]
+
+
+def build(extra_flags=(), verbose: bool = False, checked: bool = False) -> str:
+    """Build libthd.so (or, with checked, libthd_checked.so)."""
+    return _build([_variant(checked, extra_flags)], verbose)[0]
+
+
+def build_all(extra_flags=(), verbose: bool = False) -> list:
+    """Build libthd.so and libthd_checked.so together."""
+    return _build([_variant(False, extra_flags), _variant(True, extra_flags)], verbose)
 
 
 if __name__ == "__main__":
