@@ -152,7 +152,7 @@ def swap_traffic_record():
 
 def plan_kernel_name(row_bytes: int) -> str:
     """The kernel thd_swap launches for this row size (see the bulk plan in copy.cu)."""
-    if row_bytes % 16 or row_bytes < 256:
+    if row_bytes % 16 or row_bytes < 160:
         return "copy_rows_kernel<unit, SwapMap, false> (thd_swap)"
     nst = 2 if row_bytes <= 8192 else (4 if row_bytes <= 16384 else (3 if row_bytes <= 32768 else 4))
     return f"bulk_copy_kernel<{nst}, SwapMap, false> (thd_swap)"

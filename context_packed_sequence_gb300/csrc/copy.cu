@@ -5,7 +5,7 @@
 // Pure data movement, bound by HBM bandwidth.  Two engines, one row map each
 // call (linear-side row -> mapped-side row, range-checked):
 //
-//  * bulk engine (rows of >= 256 bytes, multiples of 16, 16-byte aligned
+//  * bulk engine (rows of >= 160 bytes, multiples of 16, 16-byte aligned
 //    buffers): one warp per block drives a ring of shared-memory stages with
 //    TMA bulk copies.  The linear side is cut into chunks of up to 32 rows
 //    (or row pieces); each chunk is gathered with one cp.async.bulk
@@ -33,7 +33,10 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kUnroll = 8;
 constexpr int kCopyBlocksPerSm = 3;
-constexpr int64_t kBulkMinRowBytes = 256;  // narrower rows: the unit engine
+// narrower rows: the unit engine.  On GB300 the two engines tie at 144-160 B
+// rows; from 176 B the bulk engine leads (0.85-0.94 against 0.82-0.87 of the
+// copy bandwidth), below 128 B the unit engine (0.58-0.82 against 0.14-0.76).
+constexpr int64_t kBulkMinRowBytes = 160;
 
 // ---- memory access flavours ------------------------------------------------
 

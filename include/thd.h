@@ -180,7 +180,7 @@ thd_status_t thd_partition_indices(const int32_t *cu_seqlens_padded, int32_t num
  * `row_bytes` bytes (Relax PR #273, section 2.1: pack -> all-to-all ->
  * scatter, here one pass that reads and writes every row once).
  *  src, dst   device buffers of T*row_bytes bytes that must not overlap.
- *  row_bytes  > 0.  Rows of >= 256 bytes that are a multiple of 16, with
+ *  row_bytes  > 0.  Rows of >= 160 bytes that are a multiple of 16, with
  *             16-byte aligned src/dst, move by TMA bulk copies through
  *             shared memory; other rows by 16-, 4- or 1-byte loads/stores.
  *  d_status   device int32[1] or NULL.  When given, the swap does nothing if

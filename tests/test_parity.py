@@ -185,7 +185,7 @@ def test_apply_parity(row_bytes, seed, cp, n_docs, max_chunk, empty):
         assert np.array_equal(out3.cpu().numpy(), out_o)
 
 
-@pytest.mark.parametrize("row_bytes", [256, 8192, 10240, 20480, 40960])
+@pytest.mark.parametrize("row_bytes", [144, 160, 208, 256, 8192, 10240, 20480, 40960])
 def test_apply_parity_wide_rows(row_bytes):
     """Every plan of the bulk engine: 32 rows per chunk, one row per chunk with
     2/4/3 stages, and rows cut into 16 KiB pieces."""
