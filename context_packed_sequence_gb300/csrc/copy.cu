@@ -16,9 +16,13 @@
 //    records THD_ERR_TIMEOUT, drains its own copies and returns.  Launches use
 //    programmatic dependent launch, so consecutive copies on a stream overlap
 //    launch and tail.
-//  * unit engine (everything else: narrow, odd-sized or unaligned rows): the
-//    linear side is walked as a flat array of 16-, 4- or 1-byte units, 32*U
-//    consecutive units per warp step, (row, column) kept incrementally.
+//  * run engine (rows of 16 - 144 bytes, multiples of 16, aligned): chunks
+//    of up to 512 rows; runs of rows whose mapped rows are consecutive move
+//    as single bulk copies through the same kind of ring.
+//  * unit engine (everything else: rows that are not multiples of 16 bytes,
+//    or unaligned buffers): the linear side is walked as a flat array of 4-
+//    or 1-byte units, 32*U consecutive units per warp step, (row, column)
+//    kept incrementally.
 //
 // The Ulysses exchange takes the tile transpose of ulysses_tile.cu when its
 // head-group pieces are multiples of 16 bytes below 1 KiB, these engines
@@ -33,27 +37,13 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kUnroll = 8;
 constexpr int kCopyBlocksPerSm = 3;
-// narrower rows: the unit engine.  On GB300 the two engines tie at 144-160 B
-// rows; from 176 B the bulk engine leads (0.85-0.94 against 0.82-0.87 of the
-// copy bandwidth), below 128 B the unit engine (0.58-0.82 against 0.14-0.76).
+// narrower rows: the run engine.  On GB300 the bulk engine leads the unit
+// engine from 176 B rows (0.85-0.94 against 0.82-0.87 of the copy
+// bandwidth); below 160 B the run engine (0.63-0.93) leads both.
 constexpr int64_t kBulkMinRowBytes = 160;
 
 // ---- memory access flavours ------------------------------------------------
 
-__device__ __forceinline__ uint4 load_unit(const uint4* p) {
-  uint4 v;
-  // streamed once: read-only path, do not keep in L1
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "l"(p));
-  return v;
-}
-__device__ __forceinline__ void store_unit(uint4* p, uint4 v) {
-  // streaming store: written once, not re-read by this kernel
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
 __device__ __forceinline__ uint32_t load_unit(const uint32_t* p) { return __ldg(p); }
 __device__ __forceinline__ void store_unit(uint32_t* p, uint32_t v) { *p = v; }
 __device__ __forceinline__ uint8_t load_unit(const uint8_t* p) { return __ldg(p); }
@@ -412,6 +402,217 @@ bulk_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, BulkGeom 
   if (bad) status_set(status, THD_ERR_INDEX_RANGE);
 }
 
+// ---- the run engine (rows of 16 - 144 bytes) --------------------------------
+//
+// Narrow rows move as runs: a chunk holds 32*K rows (K consecutive rows per
+// lane, about 8 KiB), every lane reads its K mapped rows, the warp finds the
+// maximal runs of rows whose mapped rows are consecutive (bit masks per lane,
+// one ballot and one shuffle for the run ends across lanes), and each run
+// moves with one bulk copy in and one out through the same ring of stages as
+// the bulk engine.  Row by row (the unit engine) such rows reach 0.58-0.81 of
+// the copy bandwidth on GB300, as runs 0.63-0.93.
+struct RunGeom {
+  int32_t rows;
+  int32_t row_bytes;
+  int32_t stage;   // bytes per stage: 32 * K rows
+  int64_t chunks;
+};
+
+template <int K, int NST, class Map, bool SCATTER>
+__global__ void __launch_bounds__(32)
+run_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, RunGeom g, Map map, int32_t* status) {
+  constexpr int CR = 32 * K;  // rows per chunk
+  extern __shared__ __align__(128) char smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(NST) * g.stage);
+  int32_t* mrows = reinterpret_cast<int32_t*>(bars + NST);  // NST x CR mapped rows
+  const int lane = threadIdx.x;
+  pdl_wait_then_release();  // launched with programmatic dependent launch
+  // one read, broadcast: the warp must take this exit together
+  if (__shfl_sync(kFull, lane == 0 ? status_load(status) : 0, 0) != 0) return;
+  const int64_t b = blockIdx.x, G = gridDim.x;
+  const int64_t n_my = g.chunks > b ? (g.chunks - b + G - 1) / G : 0;
+  if (n_my == 0) return;
+  const int64_t rb = g.row_bytes;
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  bool bad = false;
+
+  // mapped rows of this lane's K rows of chunk i (-1: out of range, -2: no row)
+  auto fetch = [&](int64_t i, int32_t (&m)[K]) {
+    const int64_t q0 = (b + i * G) * CR + lane * K;
+#pragma unroll
+    for (int k = 0; k < K; ++k) m[k] = (q0 + k < g.rows) ? map(static_cast<int32_t>(q0 + k)) : -2;
+  };
+  // Bit k of the result: row k of this lane starts no run continuing the row
+  // before it (the row is not valid, or -- on the mapped side -- its mapped
+  // row does not follow the one before, or -- on the linear side -- the row
+  // before is not valid).  *tail_end: the chunk position of the first such
+  // break after this lane's rows.
+  auto breaks = [&](const int32_t (&m)[K], bool mapped_side, uint32_t* valid_mask, int* tail_end) -> uint32_t {
+    const int32_t prev_last = __shfl_up_sync(kFull, m[K - 1], 1);
+    uint32_t brk = 0, vm = 0;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int32_t pm = k == 0 ? (lane == 0 ? -2 : prev_last) : m[k - 1];
+      const bool v = m[k] >= 0;
+      if (v) vm |= 1u << k;
+      if (!(v && pm >= 0 && (!mapped_side || m[k] == pm + 1))) brk |= 1u << k;
+    }
+    const int first = brk ? __ffs(brk) - 1 : K;
+    const uint32_t has = __ballot_sync(kFull, brk != 0);
+    const uint32_t above = lane == 31 ? 0u : (has & ~((2u << lane) - 1u));
+    const int next_lane = above ? __ffs(above) - 1 : 32;
+    const int next_first = __shfl_sync(kFull, first, next_lane < 32 ? next_lane : 0);
+    *tail_end = next_lane < 32 ? next_lane * K + next_first : CR;
+    *valid_mask = vm;
+    return brk;
+  };
+  // calls fn(position, rows) for every run that starts in this lane's rows
+  auto each_run = [&](uint32_t brk, uint32_t vm, int tail_end, auto&& fn) {
+    uint32_t starts = brk & vm;
+    while (starts) {
+      const int k = __ffs(starts) - 1;
+      starts &= starts - 1;
+      const uint32_t later = brk & ~((2u << k) - 1u);
+      const int pos = lane * K + k;
+      fn(pos, (later ? lane * K + (__ffs(later) - 1) : tail_end) - pos);
+    }
+  };
+
+  auto issue_load = [&](int64_t i, const int32_t (&m)[K]) {
+    const int s = static_cast<int>(i % NST);
+    char* st = smem + static_cast<size_t>(s) * g.stage;
+    int32_t* mr = mrows + s * CR;
+    const int64_t q0 = (b + i * G) * CR;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      mr[lane * K + k] = m[k];
+      bad |= (m[k] == -1);
+    }
+    uint32_t vm;
+    int tail_end;
+    // gather: runs of consecutive source rows; scatter: the source is linear
+    const uint32_t brk = breaks(m, !SCATTER, &vm, &tail_end);
+    const int valid_rows = __reduce_add_sync(kFull, __popc(vm));
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(valid_rows * rb));
+      maybe_stall(i, &bars[s]);
+    }
+    __syncwarp();
+    each_run(brk, vm, tail_end, [&](int pos, int n) {
+      const char* from = SCATTER ? src + (q0 + pos) * rb : src + static_cast<int64_t>(mr[pos]) * rb;
+      bulk_load(st + pos * rb, from, static_cast<uint32_t>(n * rb), &bars[s]);
+    });
+    __syncwarp();
+  };
+  auto issue_store = [&](int64_t i) {
+    const int s = static_cast<int>(i % NST);
+    const char* st = smem + static_cast<size_t>(s) * g.stage;
+    const int32_t* mr = mrows + s * CR;
+    const int64_t q0 = (b + i * G) * CR;
+    int32_t m[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) m[k] = mr[lane * K + k];
+    uint32_t vm;
+    int tail_end;
+    // gather: the destination is linear; scatter: runs of consecutive destination rows
+    const uint32_t brk = breaks(m, SCATTER, &vm, &tail_end);
+    each_run(brk, vm, tail_end, [&](int pos, int n) {
+      char* to = SCATTER ? dst + static_cast<int64_t>(mr[pos]) * rb : dst + (q0 + pos) * rb;
+      bulk_store(to, st + pos * rb, static_cast<uint32_t>(n * rb));
+    });
+    bulk_commit();
+  };
+
+  // Loads run NST-1 chunks ahead of stores, as in the bulk engine.
+  int32_t m_next[K];
+  int64_t issued = 0;
+  for (; issued < NST - 1 && issued < n_my; ++issued) {
+    fetch(issued, m_next);
+    issue_load(issued, m_next);
+  }
+  bool timed_out = false;
+  int64_t i = 0;
+  for (; i < n_my; ++i) {
+    const int64_t j = i + NST - 1;
+    if (j < n_my) fetch(j, m_next);
+    const bool landed = mbar_wait(&bars[i % NST], static_cast<uint32_t>((i / NST) & 1));
+    if (!__all_sync(kFull, landed)) {  // give up together, never with part of the warp
+      timed_out = true;
+      break;
+    }
+    issue_store(i);
+    if (j < n_my) {
+      bulk_wait_read_all_but_one();  // the store that used stage j % NST is done reading it
+      __syncwarp();
+      issue_load(j, m_next);
+      issued = j + 1;
+    }
+  }
+  if (timed_out) {
+    // let this block's copies in flight land before shared memory goes away
+    for (int64_t r = i; r < issued; ++r) mbar_wait(&bars[r % NST], static_cast<uint32_t>((r / NST) & 1));
+    if (lane == 0) status_set(status, THD_ERR_TIMEOUT);
+  }
+  bulk_wait_all();
+  if (bad) status_set(status, THD_ERR_INDEX_RANGE);
+}
+
+constexpr int kRunBlocksPerSm = 6;
+constexpr int64_t kRunStage = 8192;  // target bytes per chunk
+
+template <int K, int NST, class Map, bool SCATTER>
+thd_status_t launch_runs(const void* src, void* dst, int32_t rows, int64_t row_bytes, Map map, int32_t* status,
+                         cudaStream_t s) {
+  RunGeom g;
+  g.rows = rows;
+  g.row_bytes = static_cast<int32_t>(row_bytes);
+  g.stage = static_cast<int32_t>(32 * K * row_bytes);
+  g.chunks = (static_cast<int64_t>(rows) + 32 * K - 1) / (32 * K);
+  const size_t smem = static_cast<size_t>(NST) * g.stage + NST * (8 + 32 * K * 4);
+  cudaError_t e = cudaSuccess;
+  if (smem > 48 * 1024)
+    e = cudaFuncSetAttribute(run_copy_kernel<K, NST, Map, SCATTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (e == cudaSuccess) {
+    int64_t grid = static_cast<int64_t>(sm_count()) * kRunBlocksPerSm;
+    if (grid > g.chunks) grid = g.chunks;
+    if (grid < 1) grid = 1;
+    e = launch_pdl(run_copy_kernel<K, NST, Map, SCATTER>, dim3(static_cast<unsigned>(grid)), 32, smem, s,
+                   static_cast<const char*>(src), static_cast<char*>(dst), g, map, status);
+  }
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
+  return THD_OK;
+}
+
+// K = the largest power of two (<= 16) with 32*K rows in 8 KiB; two stages
+// when a chunk fills 8 KiB, three when it is smaller (a sweep on GB300: each
+// width's best of 2 or 3 stages follows this rule).
+template <class Map, bool SCATTER>
+thd_status_t run_runs(const void* src, void* dst, int32_t rows, int64_t row_bytes, Map map, int32_t* status,
+                      cudaStream_t s) {
+  const int64_t fit = kRunStage / (32 * row_bytes);
+  const int K = fit >= 16 ? 16 : fit >= 8 ? 8 : fit >= 4 ? 4 : fit >= 2 ? 2 : 1;
+  const bool full = 32 * K * row_bytes >= kRunStage;
+  switch (K) {
+    case 16: return full ? launch_runs<16, 2, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s)
+                         : launch_runs<16, 3, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
+    case 8: return full ? launch_runs<8, 2, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s)
+                        : launch_runs<8, 3, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
+    case 4: return full ? launch_runs<4, 2, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s)
+                        : launch_runs<4, 3, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
+    case 2: return full ? launch_runs<2, 2, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s)
+                        : launch_runs<2, 3, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
+    default: return launch_runs<1, 3, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
+  }
+}
+
 // Stage size, ring depth and blocks per SM by row size (chosen by a sweep on
 // GB300 over 4 KiB - 48 KiB stages, 2-8 stages, 1-8 blocks per SM):
 //   rows <= 8 KiB : chunks of up to 8 KiB (R rows), 2 stages, 6 blocks per SM
@@ -492,7 +693,7 @@ thd_status_t dispatch_unit(const void* src, void* dst, int32_t rows, int64_t row
   if (row_bytes % 16 == 0 && a % 16 == 0 && row_bytes >= kBulkMinRowBytes)
     return run_bulk<Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
   if (row_bytes % 16 == 0 && a % 16 == 0)
-    return run<uint4, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
+    return run_runs<Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
   if (row_bytes % 4 == 0 && a % 4 == 0)
     return run<uint32_t, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);
   return run<uint8_t, Map, SCATTER>(src, dst, rows, row_bytes, map, status, s);

@@ -180,9 +180,10 @@ thd_status_t thd_partition_indices(const int32_t *cu_seqlens_padded, int32_t num
  * `row_bytes` bytes (Relax PR #273, section 2.1: pack -> all-to-all ->
  * scatter, here one pass that reads and writes every row once).
  *  src, dst   device buffers of T*row_bytes bytes that must not overlap.
- *  row_bytes  > 0.  Rows of >= 160 bytes that are a multiple of 16, with
- *             16-byte aligned src/dst, move by TMA bulk copies through
- *             shared memory; other rows by 16-, 4- or 1-byte loads/stores.
+ *  row_bytes  > 0.  Rows that are a multiple of 16 bytes, with 16-byte
+ *             aligned src/dst, move by TMA bulk copies through shared memory
+ *             (rows of >= 160 bytes one by one, narrower rows as runs of
+ *             consecutive rows); other rows by 4- or 1-byte loads/stores.
  *  d_status   device int32[1] or NULL.  When given, the swap does nothing if
  *             it is non-zero on entry, and records THD_ERR_INDEX_RANGE.
  */
@@ -219,7 +220,7 @@ thd_status_t thd_scatter(const void *recv_buf, void *dst, int64_t row_bytes,
  *             pieces (row_bytes/cp_size) that are multiples of 16 bytes, the
  *             exchange moves by TMA bulk copies: pieces below 1 KiB (cp_size
  *             >= 2) as a tile transpose through shared memory, larger pieces
- *             one by one; other shapes by 16-, 4- or 1-byte loads and stores.
+ *             one by one or as runs; other shapes by 4- or 1-byte loads and stores.
  *  d_status   as for thd_swap.  A bad dir returns THD_ERR_BAD_DIRECTION.
  */
 thd_status_t thd_ulysses_swap(const void *src, void *dst, int64_t T, int32_t cp_size,

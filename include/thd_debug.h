@@ -15,7 +15,7 @@ extern "C" {
 
 /*
  * One-shot: block 0 of the next TMA bulk copy launched by the library (a
- * thd_swap / pack / scatter of rows of 160 bytes or more, or a Ulysses
+ * thd_swap / pack / scatter of rows that are multiples of 16 bytes, or a Ulysses
  * exchange of pieces of 1 KiB or more) waits on 16 bytes that no copy
  * delivers.  Its bounded wait runs out (about 3 s), the block lets its other
  * copies land, records THD_ERR_TIMEOUT in the call's d_status and returns;

@@ -197,16 +197,18 @@ def test_pack_docs_reports_a_too_small_output(tokens_capacity, ok):
 
 
 @pytest.mark.skipif(os.environ.get("THD_CHECKED") != "1", reason="the debug request is in the checked build only")
-def test_bulk_wait_that_runs_out_reports_timeout():
+@pytest.mark.parametrize("width", [1024, 8])
+def test_bulk_wait_that_runs_out_reports_timeout(width):
     """Block 0 of a bulk swap waits for 16 bytes that never come: its bounded
     wait gives up (about 3 s), the block lets its other copies land and
-    records THD_ERR_TIMEOUT; the next swap on the same context is exact."""
+    records THD_ERR_TIMEOUT; the next swap on the same context is exact.
+    4 KiB rows take the bulk engine, 32 B rows the run engine."""
     lib = L.load()
     stall = lib.thd_debug_stall_next_bulk_copy
     stall.restype, stall.argtypes = ctypes.c_int, [ctypes.c_void_p]
     cu = torch.tensor([0, 8, 20, 24], dtype=torch.int32, device="cuda")
     r = thd.route_build(cu, 24, 2, Z2C)
-    x = torch.arange(24 * 1024, dtype=torch.int32, device="cuda").view(24, 1024)   # 4 KiB rows: bulk engine
+    x = torch.arange(24 * width, dtype=torch.int32, device="cuda").view(24, width)
     want = x[r.src_of_dst.long()]
     st = thd.new_status()
     assert stall(torch.cuda.current_stream().cuda_stream) == L.OK

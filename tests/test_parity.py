@@ -185,10 +185,12 @@ def test_apply_parity(row_bytes, seed, cp, n_docs, max_chunk, empty):
         assert np.array_equal(out3.cpu().numpy(), out_o)
 
 
-@pytest.mark.parametrize("row_bytes", [144, 160, 208, 256, 8192, 10240, 20480, 40960])
+@pytest.mark.parametrize("row_bytes", [16, 32, 48, 64, 96, 128, 144, 160, 208, 256, 8192, 10240, 20480, 40960])
 def test_apply_parity_wide_rows(row_bytes):
-    """Every plan of the bulk engine: 32 rows per chunk, one row per chunk with
-    2/4/3 stages, and rows cut into 16 KiB pieces."""
+    """Every chunk shape of the run engine (16-144 B rows: 16, 8, 4, 2 and 1
+    rows per lane, 2 or 3 stages) and every plan of the bulk engine (32 rows
+    per chunk, one row per chunk with 2/4/3 stages, rows cut into 16 KiB
+    pieces)."""
     for seed, cp, n_docs, max_chunk, empty in [(21, 2, 30, 6, 0.1), (22, 4, 9, 5, 0.2)]:
         lens = W.random_lengths(seed, n_docs, cp, max_chunk, empty)
         cu = _bounds(lens)
@@ -267,7 +269,7 @@ def test_ulysses_fuzz():
         if case % 2:
             piece = 16 * int(rng.integers(1, 66))         # 16 .. 1040, mostly the tile transpose
         else:
-            piece = int(rng.integers(1, 300))             # odd sizes: the 16/4/1-byte unit engine
+            piece = int(rng.integers(1, 300))             # any size: run engine (multiples of 16) or unit engine
         T = cp * int(rng.integers(1, max(2, 200000 // (cp * cp * piece + 1))))
         engines.add("tile" if cp > 1 and piece % 16 == 0 and piece < 1024 else "rows")
         x_np = rng.integers(0, 256, size=(T, cp * piece), dtype=np.uint8)
