@@ -154,7 +154,7 @@ def plan_kernel_name(row_bytes: int) -> str:
     """The kernel thd_swap launches for this row size (the plans in copy.cu)."""
     if row_bytes % 16:
         return "copy_rows_kernel<unit, SwapMap, false> (thd_swap)"
-    if row_bytes < 160:
+    if row_bytes < 208:
         fit = 8192 // (32 * row_bytes)
         k = 16 if fit >= 16 else 8 if fit >= 8 else 4 if fit >= 4 else 2 if fit >= 2 else 1
         return f"run_copy_kernel<{k}, {2 if 32 * k * row_bytes >= 8192 else 3}, SwapMap, false> (thd_swap)"

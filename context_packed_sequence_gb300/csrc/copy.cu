@@ -5,7 +5,7 @@
 // Pure data movement, bound by HBM bandwidth.  Two engines, one row map each
 // call (linear-side row -> mapped-side row, range-checked):
 //
-//  * bulk engine (rows of >= 160 bytes, multiples of 16, 16-byte aligned
+//  * bulk engine (rows of >= 208 bytes, multiples of 16, 16-byte aligned
 //    buffers): one warp per block drives a ring of shared-memory stages with
 //    TMA bulk copies.  The linear side is cut into chunks of up to 32 rows
 //    (or row pieces); each chunk is gathered with one cp.async.bulk
@@ -16,7 +16,7 @@
 //    records THD_ERR_TIMEOUT, drains its own copies and returns.  Launches use
 //    programmatic dependent launch, so consecutive copies on a stream overlap
 //    launch and tail.
-//  * run engine (rows of 16 - 144 bytes, multiples of 16, aligned): chunks
+//  * run engine (rows of 16 - 192 bytes, multiples of 16, aligned): chunks
 //    of up to 512 rows; runs of rows whose mapped rows are consecutive move
 //    as single bulk copies through the same kind of ring.
 //  * unit engine (everything else: rows that are not multiples of 16 bytes,
@@ -37,10 +37,10 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kUnroll = 8;
 constexpr int kCopyBlocksPerSm = 3;
-// narrower rows: the run engine.  On GB300 the bulk engine leads the unit
-// engine from 176 B rows (0.85-0.94 against 0.82-0.87 of the copy
-// bandwidth); below 160 B the run engine (0.63-0.93) leads both.
-constexpr int64_t kBulkMinRowBytes = 160;
+// narrower rows: the run engine.  On GB300 the run engine leads at 160-192 B
+// rows (0.88-0.93 of the copy bandwidth against 0.82-0.87 row by row), the
+// bulk engine from 208 B (0.89-0.95 against 0.86-0.88).
+constexpr int64_t kBulkMinRowBytes = 208;
 
 // ---- memory access flavours ------------------------------------------------
 
@@ -402,15 +402,15 @@ bulk_copy_kernel(const char* __restrict__ src, char* __restrict__ dst, BulkGeom 
   if (bad) status_set(status, THD_ERR_INDEX_RANGE);
 }
 
-// ---- the run engine (rows of 16 - 144 bytes) --------------------------------
+// ---- the run engine (rows of 16 - 192 bytes) --------------------------------
 //
 // Narrow rows move as runs: a chunk holds 32*K rows (K consecutive rows per
 // lane, about 8 KiB), every lane reads its K mapped rows, the warp finds the
 // maximal runs of rows whose mapped rows are consecutive (bit masks per lane,
 // one ballot and one shuffle for the run ends across lanes), and each run
 // moves with one bulk copy in and one out through the same ring of stages as
-// the bulk engine.  Row by row (the unit engine) such rows reach 0.58-0.81 of
-// the copy bandwidth on GB300, as runs 0.63-0.93.
+// the bulk engine.  Row by row such rows reach 0.58-0.87 of the copy
+// bandwidth on GB300, as runs 0.63-0.93.
 struct RunGeom {
   int32_t rows;
   int32_t row_bytes;

@@ -182,7 +182,7 @@ thd_status_t thd_partition_indices(const int32_t *cu_seqlens_padded, int32_t num
  *  src, dst   device buffers of T*row_bytes bytes that must not overlap.
  *  row_bytes  > 0.  Rows that are a multiple of 16 bytes, with 16-byte
  *             aligned src/dst, move by TMA bulk copies through shared memory
- *             (rows of >= 160 bytes one by one, narrower rows as runs of
+ *             (rows of >= 208 bytes one by one, narrower rows as runs of
  *             consecutive rows); other rows by 4- or 1-byte loads/stores.
  *  d_status   device int32[1] or NULL.  When given, the swap does nothing if
  *             it is non-zero on entry, and records THD_ERR_INDEX_RANGE.

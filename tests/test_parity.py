@@ -185,9 +185,9 @@ def test_apply_parity(row_bytes, seed, cp, n_docs, max_chunk, empty):
         assert np.array_equal(out3.cpu().numpy(), out_o)
 
 
-@pytest.mark.parametrize("row_bytes", [16, 32, 48, 64, 96, 128, 144, 160, 208, 256, 8192, 10240, 20480, 40960])
+@pytest.mark.parametrize("row_bytes", [16, 32, 48, 64, 96, 128, 144, 160, 192, 208, 256, 8192, 10240, 20480, 40960])
 def test_apply_parity_wide_rows(row_bytes):
-    """Every chunk shape of the run engine (16-144 B rows: 16, 8, 4, 2 and 1
+    """Every chunk shape of the run engine (16-192 B rows: 16, 8, 4, 2 and 1
     rows per lane, 2 or 3 stages) and every plan of the bulk engine (32 rows
     per chunk, one row per chunk with 2/4/3 stages, rows cut into 16 KiB
     pieces)."""
