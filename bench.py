@@ -468,6 +468,36 @@ def run_thd(args, rank, world, local):
                "gbs": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3, 1),
                "frac_of_measured": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3 / peak_gbs, 4)}
 
+    # the pages' three passes (pack -> all-to-all -> scatter) for one z->c
+    # conversion, reported against the fused swap's algorithmic bytes
+    unfused = None
+    if layers > 0:
+        send, recv = torch.empty_like(x), torch.empty_like(x)
+        ts = []
+        for it in range(25):
+            if it == 0 or it % 5 == 0:
+                torch.cuda._sleep(200_000)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            lib.thd_pack(x.data_ptr(), send.data_ptr(), row_bytes, ctypes.byref(fwd.c), status.data_ptr(), sp)
+            lib.thd_a2a_local(send.data_ptr(), recv.data_ptr(), row_bytes, ctypes.byref(fwd.c), status.data_ptr(), sp)
+            lib.thd_scatter(recv.data_ptr(), y.data_ptr(), row_bytes, ctypes.byref(fwd.c), status.data_ptr(), sp)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            if it >= 5:
+                ts.append(a.elapsed_time(b) * 1e3)
+        lib.thd_swap(x.data_ptr(), send.data_ptr(), row_bytes, ctypes.byref(fwd.c), status.data_ptr(), sp)
+        torch.cuda.synchronize(device)
+        if thd.status_read(status) != 0 or not torch.equal(send, y):
+            raise RuntimeError("the three passes and the fused swap disagree")
+        del send, recv
+        t3 = statistics.median(ts)
+        peak_gbs, _ = measured_peak()
+        unfused = {"pack_a2a_scatter_us": round(t3, 2), "payload_passes": 3,
+                   "gbs": round(swap_bytes / t3 / 1e3, 1),
+                   "frac_of_measured": round(swap_bytes / t3 / 1e3 / peak_gbs, 4),
+                   "vs_fused": "same algorithmic bytes (2 x T x row_bytes) as one fused swap"}
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -520,6 +550,8 @@ def run_thd(args, rank, world, local):
         "gpu_launches": launches_per_step * n_ev * world,   # every rank's, like value
         "clocks": clock_rec,
     }
+    if unfused is not None:
+        result["unfused"] = unfused
     if e2e is not None:
         result["e2e"] = e2e
     if prep is not None:
