@@ -459,10 +459,13 @@ def run_thd(args, rank, world, local):
         if thd.status_read(status) != 0:
             raise RuntimeError("device status set by the Ulysses exchange")
         piece = row_bytes // cp
-        # the library's rule (copy.cu / ulysses_tile.cu): pieces that are
-        # multiples of 16 bytes below 1 KiB take the tile transpose
-        engine = ("tile transpose (ulysses_to_heads_kernel / ulysses_to_sequence_kernel)"
-                  if cp > 1 and piece % 16 == 0 and piece < 1024 else "row engine")
+        # the library's rule (ulysses_tile.cu): pieces that are multiples of
+        # 16 bytes below 256 B take the tile transpose, 256 B - 1 KiB take it
+        # when a tile holds enough tokens, the rest go piece by piece
+        tiled = cp > 1 and piece % 16 == 0
+        engine = ("tile transpose (ulysses_to_heads_kernel / ulysses_to_sequence_kernel)" if tiled and piece < 256
+                  else "tile transpose or row engine, by tokens per tile" if tiled and piece < 1024
+                  else "row engine")
         uly = {"piece_bytes": piece, "engine": engine, "seq_to_head_us": round(to_head, 2),
                "head_to_seq_us": round(to_seq, 2),
                "gbs": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3, 1),

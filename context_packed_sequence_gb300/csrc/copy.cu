@@ -704,7 +704,7 @@ thd_status_t dispatch_unit(const void* src, void* dst, int32_t rows, int64_t row
 thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes, bool seq_to_head,
                             int32_t* status, cudaStream_t s) {
   if (T == 0) return THD_OK;
-  if (ulysses_tiles_apply(src, dst, T, cp, row_bytes))  // small head groups: tile transpose
+  if (ulysses_tiles_apply(src, dst, T, cp, row_bytes, seq_to_head))  // small head groups: tile transpose
     return launch_ulysses_tiles(src, dst, T, cp, row_bytes, seq_to_head, status, s);
   const UlyssesMap map{T, cp, seq_to_head, make_fast_div(seq_to_head ? T : cp)};
   return dispatch_unit<UlyssesMap, false>(src, dst, T * cp, row_bytes / cp, map, status, s);

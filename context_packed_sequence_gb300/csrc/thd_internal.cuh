@@ -406,7 +406,8 @@ thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, i
                             int32_t* status, cudaStream_t s);
 // tile transpose for head-group pieces below 1 KiB (multiples of 16 bytes,
 // 16-byte aligned buffers); ulysses_tiles_apply says whether it takes the call
-bool ulysses_tiles_apply(const void* src, const void* dst, int32_t T, int32_t cp, int64_t row_bytes);
+bool ulysses_tiles_apply(const void* src, const void* dst, int32_t T, int32_t cp, int64_t row_bytes,
+                         bool seq_to_head);
 thd_status_t launch_ulysses_tiles(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes,
                                   bool seq_to_head, int32_t* status, cudaStream_t s);
 thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, const int32_t* cu,

@@ -6,8 +6,8 @@
 // head group; the head-sharded buffer holds, for each group h, every token's
 // piece h contiguously ([cp][T][P]).  Gathering pieces one by one (the row
 // engines in copy.cu) moves P bytes per copy, so small pieces leave HBM idle
-// between requests.  Here a tile of R consecutive tokens (about 24 KiB) moves
-// as a few large bulk copies instead:
+// between requests.  Here a tile of R consecutive tokens (24-44 KiB, chosen
+// by cp and direction in tile_target) moves as a few large bulk copies instead:
 //
 //   sequence -> head (ulysses_to_heads_kernel): one bulk load of the tile's R
 //     token rows (R*cp*P contiguous bytes), a shared-memory transpose into cp
@@ -37,9 +37,8 @@
 namespace thd {
 namespace {
 
-constexpr int kTileStages = 3;              // load buffers; two more for stores
-constexpr int64_t kTileTarget = 24 * 1024;  // bytes of token rows per tile
-constexpr int64_t kTileMaxPiece = 1024;     // larger pieces: the bulk row engine
+constexpr int kTileStages = 3;           // load buffers; two more for stores
+constexpr int64_t kTileMaxPiece = 1024;  // larger pieces: the bulk row engine
 constexpr size_t kTileSmemLimit = 227 * 1024;
 constexpr int kTransposers = 256;                      // threads that transpose a tile
 constexpr int kToSequenceThreads = 32 + kTransposers;  // + the loading warp
@@ -64,12 +63,27 @@ struct TileGeom {
   FastDiv div_piece;  // by upr
 };
 
-TileGeom tile_geom(int32_t T, int32_t cp, int64_t row_bytes) {
+// Bytes of token rows per tile.  Swept on GB300 over cp = 2-64 and tiles of
+// 16-44 KiB (pieces of 32 and 64 B, 0.5 GiB buffers; the throughput depends
+// on cp and the tile, hardly on the piece): 24 KiB is best for cp <= 12 in
+// both directions (0.93-0.96 of the copy bandwidth, 0.87-0.91 at 28-44 KiB);
+// above that each direction has its own best tile, which grows with cp:
+// sequence -> head 28 KiB at cp = 16 (0.94 against 0.90 at 24 KiB), 32 KiB at
+// cp = 24 (0.93 against 0.77), 40 KiB at cp = 32 (0.92 against 0.67); head ->
+// sequence 28 KiB at cp = 24 (0.94 against 0.91), 32 KiB at cp = 32 (0.95
+// against 0.81).  At cp = 64 the largest tile that fits does best (0.66-0.75).
+int64_t tile_target(int32_t cp, bool seq_to_head) {
+  constexpr int64_t K = 1024;
+  if (seq_to_head) return cp <= 12 ? 24 * K : cp <= 16 ? 28 * K : cp <= 24 ? 32 * K : cp <= 32 ? 40 * K : 44 * K;
+  return cp <= 16 ? 24 * K : cp <= 24 ? 28 * K : cp <= 32 ? 32 * K : 44 * K;
+}
+
+TileGeom tile_geom(int32_t T, int32_t cp, int64_t row_bytes, int64_t target) {
   TileGeom g;
   g.T = T;
   g.cp = cp;
   g.upr = static_cast<int32_t>(row_bytes / cp / 16);
-  int64_t R = kTileTarget / row_bytes;
+  int64_t R = target / row_bytes;
   if (R < 1) R = 1;
   g.R = static_cast<int32_t>(R);
   const int64_t pad = ((g.upr - R * g.upr) % 8 + 8) % 8;  // makes H16 = upr (mod 8)
@@ -84,6 +98,17 @@ TileGeom tile_geom(int32_t T, int32_t cp, int64_t row_bytes) {
 // buffers, then one "loaded" and one "released" mbarrier per load buffer
 size_t tile_smem(const TileGeom& g) {
   return static_cast<size_t>(kTileStages + 2) * g.stage + 2 * kTileStages * sizeof(uint64_t);
+}
+
+// The geometry for (cp, direction): the tile of tile_target, 4 KiB smaller
+// at a time while its buffers do not fit in shared memory.  False when not
+// even one token row per tile fits.
+bool pick_geom(int32_t T, int32_t cp, int64_t row_bytes, bool seq_to_head, TileGeom* g) {
+  for (int64_t target = tile_target(cp, seq_to_head);; target -= 4096) {
+    *g = tile_geom(T, cp, row_bytes, target);
+    if (tile_smem(*g) <= kTileSmemLimit) return true;
+    if (g->R == 1) return false;
+  }
 }
 
 // The tiles of block b: tile b + i*G covers tokens [start(i), start(i) + rows(i)).
@@ -321,17 +346,30 @@ thd_status_t launch_tiles(Kernel kernel, int threads, const void* src, void* dst
 
 }  // namespace
 
-bool ulysses_tiles_apply(const void* src, const void* dst, int32_t T, int32_t cp, int64_t row_bytes) {
+bool ulysses_tiles_apply(const void* src, const void* dst, int32_t T, int32_t cp, int64_t row_bytes,
+                         bool seq_to_head) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
   if (cp < 2 || T <= 0 || a % 16 != 0 || row_bytes % cp != 0) return false;
   const int64_t P = row_bytes / cp;
   if (P % 16 != 0 || P >= kTileMaxPiece) return false;
-  return tile_smem(tile_geom(T, cp, row_bytes)) <= kTileSmemLimit;
+  TileGeom g;
+  if (!pick_geom(T, cp, row_bytes, seq_to_head, &g)) return false;
+  // Pieces of 256 B and more also go well piece by piece (0.83-0.91 of the
+  // copy bandwidth through the bulk row engine), and a tile of them holds few
+  // tokens, so its runs are short.  Measured on GB300 (cp = 16-64, pieces of
+  // 256-768 B), the tile transpose wins when sequence -> head tiles hold at
+  // least 4 tokens (cp = 32, 256 B: 0.93 against 0.84) and loses below (cp =
+  // 32, 512 B: 0.83 against 0.90; cp = 64, 256 B: 0.54 against 0.84); head ->
+  // sequence wins with 2 tokens when the runs reach 640 B (cp = 32, 512 B:
+  // 0.95 against 0.90) and loses below (cp = 64, 256 B: 0.59 against 0.83).
+  if (P < 256) return true;
+  return seq_to_head ? g.R >= 4 : g.R >= 2 && g.R * P >= 640;
 }
 
 thd_status_t launch_ulysses_tiles(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes,
                                   bool seq_to_head, int32_t* status, cudaStream_t s) {
-  const TileGeom g = tile_geom(T, cp, row_bytes);
+  TileGeom g;
+  if (!pick_geom(T, cp, row_bytes, seq_to_head, &g)) return THD_ERR_INVALID_ARG;
   const size_t smem = tile_smem(g);
   return seq_to_head ? launch_tiles(ulysses_to_heads_kernel, kTransposers, src, dst, g, smem, status, s)
                      : launch_tiles(ulysses_to_sequence_kernel, kToSequenceThreads, src, dst, g, smem, status, s);

@@ -241,6 +241,9 @@ def test_unaligned_buffers_take_the_narrow_path():
     (32, 64, 32, 1008),      # rows of 31.5 KiB: one token per tile
     (64, 64, 64, 1008),      # a tile would not fit in shared memory: bulk row engine
     (64, 128, 64, 16),       # cp = 64: each issuing lane takes two runs
+    (24, 24 * 411, 24, 32),  # cp = 24: 32/28 KiB tiles, ragged last tile
+    (32, 32 * 397, 32, 16),  # cp = 32: 40/32 KiB tiles, ragged last tile
+    (64, 64 * 101, 64, 32),  # cp = 64: the 44 KiB tile shrunk to 40 KiB to fit
 ])
 def test_ulysses_parity(cp, T, heads, head_bytes):
     rng = np.random.default_rng(cp * 100 + T)
@@ -259,9 +262,9 @@ def test_ulysses_parity(cp, T, heads, head_bytes):
 
 def test_ulysses_fuzz():
     """40 random shapes through every engine of the exchange: cp 1-16, pieces
-    of 1-1040 bytes (multiples of 16 below 1 KiB take the tile transpose,
-    larger or odd ones the row engines), token counts that leave ragged last
-    tiles; both directions against the oracle."""
+    of 1-1040 bytes (multiples of 16 below 1 KiB mostly take the tile
+    transpose, larger or odd ones the row engines), token counts that leave
+    ragged last tiles; both directions against the oracle."""
     rng = np.random.default_rng(2027)
     engines = set()
     for case in range(40):
