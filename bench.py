@@ -381,6 +381,35 @@ def run_thd(args, rank, world, local):
     route_us = {k: round(statistics.median(v), 2) for k, v in rb.items()}
     route_us["method"] = "median of 50, CUDA events with the GPU kept busy ahead of each launch"
 
+    # The same kernels' own duration: 20 launches back to back between two
+    # events (each waits for the previous one, so launch latency overlaps
+    # the previous launch), per launch, median of 20.  Single-launch events
+    # move in steps of about 2 us on this GPU; this figure resolves below that.
+    calls = {
+        "both_directions": lambda: lib.thd_route_build_pair(cu_d.data_ptr(), n_docs, T, cp, ctypes.byref(fwd.c),
+                                                            ctypes.byref(bwd.c), status.data_ptr(), sp),
+        "zigzag_to_contiguous": lambda: lib.thd_route_build(cu_d.data_ptr(), n_docs, T, cp, 0, ctypes.byref(fwd.c),
+                                                            status.data_ptr(), sp),
+        "contiguous_to_zigzag": lambda: lib.thd_route_build(cu_d.data_ptr(), n_docs, T, cp, 1, ctypes.byref(bwd.c),
+                                                            status.data_ptr(), sp),
+        "partition": lambda: lib.thd_partition_indices(cu_d.data_ptr(), n_docs, T, cp, -1, pidx.data_ptr(),
+                                                       status.data_ptr(), sp),
+    }
+    b2b = {name: [] for name in calls}
+    for it in range(23):
+        for name, fn in calls.items():
+            torch.cuda._sleep(200_000)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(20):
+                fn()
+            ev1.record(stream)
+            torch.cuda.synchronize(device)
+            if it >= 3:
+                b2b[name].append(ev0.elapsed_time(ev1) * 1e3 / 20)
+    route_us["back_to_back"] = {k: round(statistics.median(v), 2) for k, v in b2b.items()}
+    route_us["back_to_back_method"] = "20 launches between two CUDA events, per launch, median of 20"
+
     # packing and labels alone (pipeline workload): CUDA events, median of 20
     prep = None
     if extra is not None:

@@ -9,7 +9,8 @@
 // tokens[p+1+k] at depth k when p+1+k is still before the document's valid
 // end e_i, else `fill` with mask 0.  Warps walk contiguous position ranges
 // and follow the current document forward, so finding it costs a step or
-// two per 32 positions instead of a full search per position.
+// two per 32 positions instead of a full search per position; the zigzag
+// variant walks slot tiles shared by every rank, as the route build does.
 #include "thd_internal.cuh"
 
 namespace thd {
@@ -17,6 +18,10 @@ namespace {
 
 constexpr int kLabelThreads = 512;
 constexpr int kSmemBudget = 48 * 1024;
+// At most this many blocks per SM for the zigzag variant's slot-tile walk.
+#ifndef THD_LABEL_ZZ_BLOCKS_PER_SM
+#define THD_LABEL_ZZ_BLOCKS_PER_SM 2
+#endif
 
 // Optional continuation of a document cut by the end of its sample (the
 // sample's extra token, "Packed Sequence 与上下文并行" section 1.3): when
@@ -60,8 +65,8 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
   extern __shared__ int32_t smem[];
   const int32_t* unused;
   pdl_wait_then_release();
+  if (SMEM_CU) stage_rows(cu_v_g, n + 1, smem + (n + 1));  // covered by the barrier below
   if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
-  stage_cu(cu_v_g, n, smem + (n + 1), SMEM_CU);
   const int32_t* cu = SMEM_CU ? smem : cu_g;
   const int32_t* cu_v = SMEM_CU ? smem + (n + 1) : cu_v_g;
 
@@ -115,14 +120,14 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
 template <bool SMEM_CU>
 __global__ void __launch_bounds__(kLabelThreads)
 roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
-                          int32_t n, int32_t T, CpMath m, FastDiv divS, int32_t depth, int32_t fill, NextTokens next,
+                          int32_t n, int32_t T, CpMath m, int32_t depth, int32_t fill, NextTokens next,
                           int32_t* __restrict__ labels, uint8_t* __restrict__ lmask, uint8_t* __restrict__ valid,
                           int32_t* status) {
   extern __shared__ int32_t smem[];
   const int32_t* unused;
   pdl_wait_then_release();
+  if (SMEM_CU) stage_rows(cu_v_g, n + 1, smem + (n + 1));  // covered by the barrier below
   if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
-  stage_cu(cu_v_g, n, smem + (n + 1), SMEM_CU);
   const int32_t* cu = SMEM_CU ? smem : cu_g;
   const int32_t* cu_v = SMEM_CU ? smem + (n + 1) : cu_v_g;
 
@@ -140,19 +145,29 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
     if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
     return;
   }
+  // (slot tile, rank) items as in the route build: a tile's documents and
+  // valid ends are found once and serve every rank's row of each slot
   const int32_t S = T / m.cp;
+  const int64_t tiles = (static_cast<int64_t>(S) + 31) / 32;
   int64_t begin, end;
-  warp_range(T, &begin, &end);
-  const int32_t lane = threadIdx.x & 31;
-  TileWalker w{0, -1};
-  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
-    const TileRow t = tile_row(cu, n, m, S, divS, static_cast<int32_t>(tile0) + lane,
-                               static_cast<int32_t>(end) - 1, w);
-    if (t.u < end && in_range(t.doc, 0, n, status) && in_range(t.g, 0, T, status)) {
-      const int32_t e = cu[t.doc] + (cu_v[t.doc + 1] - cu_v[t.doc]);
-      if (!in_range(e, 0, static_cast<int64_t>(T) + 1, status)) continue;  // token reads stay below e
-      valid[t.u] = t.g < e ? 1 : 0;
-      write_targets(tokens, next, t.doc, t.g, t.u, e, depth, fill, T, labels, lmask);
+  warp_items(tiles * m.cp, 1, &begin, &end);
+  if (begin >= end) return;
+  int32_t wdoc = -1;
+  const int32_t t_last = static_cast<int32_t>((end - 1) / m.cp);
+  for (int32_t tile = static_cast<int32_t>(begin / m.cp); tile <= t_last; ++tile) {
+    const SlotTile t = slot_tile(cu, n, m, S, tile, wdoc);
+    const int64_t q0 = static_cast<int64_t>(tile) * m.cp;
+    const int32_t r0 = static_cast<int32_t>(max(begin - q0, int64_t{0}));
+    const int32_t r1 = static_cast<int32_t>(min(end - q0, static_cast<int64_t>(m.cp)));
+    if (!t.valid || !in_range(t.doc, 0, n, status)) continue;
+    const int32_t e = cu[t.doc] + (cu_v[t.doc + 1] - cu_v[t.doc]);  // end of the document's valid tokens
+    if (!in_range(e, 0, static_cast<int64_t>(T) + 1, status)) continue;  // token reads stay below e
+    for (int32_t r = r0; r < r1; ++r) {
+      const int32_t g = t.base + r * t.step;
+      const int32_t u = r * S + t.j;
+      if (!in_range(g, 0, T, status)) continue;
+      valid[u] = g < e ? 1 : 0;
+      write_targets(tokens, next, t.doc, g, u, e, depth, fill, T, labels, lmask);
     }
   }
 }
@@ -167,18 +182,16 @@ thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_
   size_t bytes = static_cast<size_t>(2) * (n + 1) * sizeof(int32_t);
   bool in_smem = bytes <= static_cast<size_t>(kSmemBudget);
   int64_t grid = (static_cast<int64_t>(T) + kLabelThreads - 1) / kLabelThreads;
-  int64_t cap = static_cast<int64_t>(sm_count()) * 2;
+  int64_t cap = static_cast<int64_t>(sm_count()) * THD_LABEL_ZZ_BLOCKS_PER_SM;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  const int32_t S = T / cp;
   const CpMath m = make_cp_math(cp);
-  const FastDiv divS = make_fast_div(S > 0 ? S : 1);
   const dim3 blocks(static_cast<unsigned>(grid));
   const cudaError_t e =
       in_smem ? launch_pdl(roll_labels_zigzag_kernel<true>, blocks, kLabelThreads, bytes, s, tokens, cu_v, cu, n, T,
-                           m, divS, depth, fill, next, labels, lmask, valid, status)
+                           m, depth, fill, next, labels, lmask, valid, status)
               : launch_pdl(roll_labels_zigzag_kernel<false>, blocks, kLabelThreads, 0, s, tokens, cu_v, cu, n, T, m,
-                           divS, depth, fill, next, labels, lmask, valid, status);
+                           depth, fill, next, labels, lmask, valid, status);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

@@ -5,15 +5,17 @@
 // follows from interval intersection.  The pages copy cu_seqlens to the host
 // and intersect with a Python two-pointer loop.  Here one kernel per call:
 //
-//  1. every block stages the boundaries in shared memory, validates them
-//     (all blocks reach the same verdict; block 0 writes the status word) and
-//     derives the cp x (cp+1) table "zigzag rows of rank s below d*S" in
-//     closed form, plus the receive offsets;
-//  2. warps walk the zigzag buffer in tiles of 32 consecutive positions
-//     (rank r, slot j).  A tile's documents come from one full search of the
-//     boundaries plus a short window search per lane; the global row g, the
-//     contiguous rank of g and the entry's place in every route array then
-//     follow in closed form, with divisions by S done by multiply-shift.
+//  1. every block stages the boundaries in shared memory and validates them
+//     in one pass (all blocks reach the same verdict; block 0 writes the
+//     status word), then derives the cp x (cp+1) tables "zigzag rows of rank
+//     s below d*S" and the receive offsets, each entry in closed form;
+//  2. warps walk the zigzag layout in slot tiles: 32 consecutive local slots
+//     whose documents are found once (a galloping search forward from the
+//     previous tile plus a short window search per lane) and then serve every
+//     rank, since all ranks' shards share the documents' slot ranges.  The
+//     global row of each (rank, slot), its contiguous rank and the entry's
+//     place in every route array follow in closed form, with divisions by S
+//     done by multiply-shift.
 //
 // No host synchronisation, no atomics on the route, deterministic.
 #include "thd_internal.cuh"
@@ -23,6 +25,20 @@ namespace {
 
 constexpr int kRouteThreads = 512;
 constexpr int kSmemBudget = 48 * 1024;
+// Launch shape of the walking kernels: blocks per SM at most, and the least
+// number of (slot tile, rank) items a warp takes.
+#ifndef THD_ROUTE_BLOCKS_PER_SM
+#define THD_ROUTE_BLOCKS_PER_SM 1
+#endif
+#ifndef THD_ROUTE_MIN_ITEMS
+#define THD_ROUTE_MIN_ITEMS 1
+#endif
+// Ranks of one slot tile handled together by a lane (independent chains of
+// arithmetic, table loads and stores that overlap).
+#ifndef THD_ROUTE_UNROLL
+#define THD_ROUTE_UNROLL 1
+#endif
+constexpr int kRouteUnroll = THD_ROUTE_UNROLL;
 
 struct RouteArgs {
   const int32_t* cu;
@@ -97,34 +113,59 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   const int32_t cp = m.cp, S = a.S, T = a.T, n = a.n;
   int32_t* cnt = smem;                        // [cp][cp+1]: zigzag rows of s below d*S
   int32_t* roff = cnt + cp * (cp + 1);        // [d][cp+1]: z->c receive offsets
-  int32_t* cu_s = roff + cp * (cp + 1);
-  const int32_t* unused;
+  int32_t* bnd = roff + cp * (cp + 1);        // [3][cp+1]: document start, chunk, offset at d*S
+  int32_t* cu_s = bnd + 3 * (cp + 1);
   pdl_wait_then_release();
-  if (stage_cu_check_status(a.cu, n, cu_s, SMEM_CU, a.status, &unused)) return;
-  const int32_t* cu = SMEM_CU ? cu_s : a.cu;
-
-  int32_t code = block_check_cu(cu, n, T, 2 * cp, true);
+  const int32_t code = stage_check_cu(a.cu, n, cu_s, SMEM_CU, a.status, T, 2 * cp);
   if (code != THD_OK) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) status_set(a.status, code);
+    if (code != kStatusWasSet && blockIdx.x == 0 && threadIdx.x == 0) status_set(a.status, code);
     return;
   }
+  const int32_t* cu = SMEM_CU ? cu_s : a.cu;
 
-  for (int32_t e = threadIdx.x; e < cp * (cp + 1); e += blockDim.x) {
-    int32_t s = e / (cp + 1), d = e - s * (cp + 1);
-    cnt[e] = zigzag_count_below(cu, n, m, S, T, s, d * S);
-  }
-  __syncthreads();
-  for (int32_t d = threadIdx.x; d < cp; d += blockDim.x) {
-    int32_t acc = 0;
-    for (int32_t s = 0; s < cp; ++s) {
-      roff[d * (cp + 1) + s] = acc;
-      acc += cnt[s * (cp + 1) + d + 1] - cnt[s * (cp + 1) + d];
+  // Both tables in closed form from the document holding each contiguous
+  // boundary X_d = d*S (one search per boundary): its start c0, chunk length
+  // c and offset off = X_d - c0 (c = -1 marks X_d = T).  Then
+  //   cnt[s][d]  = zigzag rows of rank s below X_d
+  //              = c0/cp + clip(off - s*c) + clip(off - (2cp-1-s)*c), clip to [0, c];
+  //   roff[d][s] = rows ranks 0..s-1 send to contiguous rank d = P(s, X_{d+1}) - P(s, X_d)
+  //   with P(s, X) = rows of ranks < s below X
+  //              = s*c0/cp + min(off, s*c) + max(0, off - (2cp-s)*c)
+  //   (ranks below s own chunks [0, s) and [2cp-s, 2cp) of every document).
+  for (int32_t d = threadIdx.x; d <= cp; d += blockDim.x) {
+    const int32_t X = d * S;
+    if (X >= T) {
+      bnd[d] = 0, bnd[(cp + 1) + d] = -1, bnd[2 * (cp + 1) + d] = 0;
+    } else {
+      const int32_t i = doc_of(cu, n, X);
+      bnd[d] = cu[i];
+      bnd[(cp + 1) + d] = m.div2(cu[i + 1] - cu[i]);
+      bnd[2 * (cp + 1) + d] = X - cu[i];
     }
-    roff[d * (cp + 1) + cp] = acc;
+  }
+  __syncthreads();
+  for (int32_t e = threadIdx.x; e < cp * (cp + 1); e += blockDim.x) {
+    const int32_t x = e / (cp + 1), y = e - x * (cp + 1);
+    {  // cnt[s = x][d = y]
+      const int32_t c = bnd[(cp + 1) + y], off = bnd[2 * (cp + 1) + y];
+      cnt[e] = c < 0 ? S
+                     : m.div(bnd[y]) + min(max(off - x * c, 0), c) + min(max(off - (2 * cp - 1 - x) * c, 0), c);
+    }
+    {  // roff[d = x][s = y]
+      int32_t p[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int32_t b = x + 1 - k;  // boundary X_{d+1}, then X_d
+        const int32_t c = bnd[(cp + 1) + b], off = bnd[2 * (cp + 1) + b];
+        p[k] = c < 0 ? y * S : y * m.div(bnd[b]) + min(off, y * c) + max(0, off - (2 * cp - y) * c);
+      }
+      roff[e] = p[0] - p[1];
+    }
   }
   __syncthreads();
 
-  if (blockIdx.x == 0) {
+  // the last block has the fewest walk items (equal shares, remainder last)
+  if (blockIdx.x == gridDim.x - 1) {
     if (DIRS & kZC) write_small_arrays(a.zc, true, cu, n, m, S, cnt, roff);
     if (DIRS & kCZ) write_small_arrays(a.cz, false, cu, n, m, S, cnt, roff);
   }
@@ -135,27 +176,36 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   //   with d = g / S the contiguous rank of g, the row is entry
   //   roff[d][r] + (j - cnt[r][d]) of d's z->c receive buffer and of d's c->z
   //   send buffer, with value g - d*S.
+  const int64_t tiles = (static_cast<int64_t>(S) + 31) / 32;
   int64_t begin, end;
-  warp_range(T, &begin, &end);
+  warp_items(tiles * cp, THD_ROUTE_MIN_ITEMS, &begin, &end);
+  if (begin >= end) return;
   const FastDiv divS = a.divS;
-  const int32_t lane = threadIdx.x & 31;
-  TileWalker w{0, -1};
-  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
-    const TileRow t = tile_row(cu, n, m, S, divS, static_cast<int32_t>(tile0) + lane,
-                               static_cast<int32_t>(end) - 1, w);
-    if (t.u < end && in_range(t.doc, 0, n, a.status) && in_range(t.g, 0, T, a.status)) {
-      const int32_t d = divS.div(t.g);
-      const int32_t pos = d * S + roff[d * (cp + 1) + t.r] + (t.j - cnt[t.r * (cp + 1) + d]);
+  int32_t wdoc = -1;
+  const int32_t t_last = static_cast<int32_t>((end - 1) / cp);
+  for (int32_t tile = static_cast<int32_t>(begin / cp); tile <= t_last; ++tile) {
+    const SlotTile t = slot_tile(cu, n, m, S, tile, wdoc);
+    const int64_t q0 = static_cast<int64_t>(tile) * cp;
+    const int32_t r0 = static_cast<int32_t>(max(begin - q0, int64_t{0}));
+    const int32_t r1 = static_cast<int32_t>(min(end - q0, static_cast<int64_t>(cp)));
+    if (!t.valid || !in_range(t.doc, 0, n, a.status)) continue;
+#pragma unroll kRouteUnroll
+    for (int32_t r = r0; r < r1; ++r) {
+      const int32_t g = t.base + r * t.step;
+      const int32_t u = r * S + t.j;
+      if (!in_range(g, 0, T, a.status)) continue;
+      const int32_t d = divS.div(g);
+      const int32_t pos = d * S + roff[d * (cp + 1) + r] + (t.j - cnt[r * (cp + 1) + d]);
       if (!in_range(pos, d * static_cast<int64_t>(S), (d + 1) * static_cast<int64_t>(S), a.status)) continue;
       if (DIRS & kZC) {
-        a.zc.src_of_dst[t.g] = t.u;
-        a.zc.send_rows[t.u] = t.j;
-        a.zc.recv_rows[pos] = t.g - d * S;
+        a.zc.src_of_dst[g] = u;
+        a.zc.send_rows[u] = t.j;
+        a.zc.recv_rows[pos] = g - d * S;
       }
       if (DIRS & kCZ) {
-        a.cz.src_of_dst[t.u] = t.g;
-        a.cz.recv_rows[t.u] = t.j;
-        a.cz.send_rows[pos] = t.g - d * S;
+        a.cz.src_of_dst[u] = g;
+        a.cz.recv_rows[u] = t.j;
+        a.cz.send_rows[pos] = g - d * S;
       }
     }
   }
@@ -163,36 +213,46 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
 
 template <bool SMEM_CU>
 __global__ void __launch_bounds__(kRouteThreads)
-partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, CpMath m, FastDiv divS, int32_t S, int32_t rank,
+partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, CpMath m, int32_t S, int32_t rank,
                  int32_t* out, int32_t* status) {
   extern __shared__ int32_t smem[];
-  const int32_t* unused;
   pdl_wait_then_release();
-  if (stage_cu_check_status(cu_g, n, smem, SMEM_CU, status, &unused)) return;
-  const int32_t* cu = SMEM_CU ? smem : cu_g;
-  int32_t code = block_check_cu(cu, n, T, 2 * m.cp, true);
+  const int32_t code = stage_check_cu(cu_g, n, smem, SMEM_CU, status, T, 2 * m.cp);
   if (code != THD_OK) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
+    if (code != kStatusWasSet && blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
     return;
   }
-  // all ranks: out[u] for zigzag positions u in [0, T); one rank r: out[j]
-  // for positions r*S + j, j in [0, S)
-  const int32_t total = rank < 0 ? T : S;
-  const int32_t base = rank < 0 ? 0 : rank * S;
+  const int32_t* cu = SMEM_CU ? smem : cu_g;
+  // all ranks: out[r*S + j] for every (slot tile, rank) item; one rank r:
+  // out[j], one item per slot tile
+  const int32_t nr = rank < 0 ? m.cp : 1;
+  const int32_t r_base = rank < 0 ? 0 : rank;
+  const int64_t tiles = (static_cast<int64_t>(S) + 31) / 32;
   int64_t begin, end;
-  warp_range(total, &begin, &end);
-  const int32_t lane = threadIdx.x & 31;
-  TileWalker w{0, -1};
-  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
-    const int32_t k = static_cast<int32_t>(tile0) + lane;
-    const TileRow t = tile_row(cu, n, m, S, divS, base + k, base + static_cast<int32_t>(end) - 1, w);
-    if (k < end && in_range(t.g, 0, T, status)) out[k] = t.g;
+  warp_items(tiles * nr, THD_ROUTE_MIN_ITEMS, &begin, &end);
+  if (begin >= end) return;
+  int32_t wdoc = -1;
+  const int32_t t_last = static_cast<int32_t>((end - 1) / nr);
+  for (int32_t tile = static_cast<int32_t>(begin / nr); tile <= t_last; ++tile) {
+    const SlotTile t = slot_tile(cu, n, m, S, tile, wdoc);
+    const int64_t q0 = static_cast<int64_t>(tile) * nr;
+    const int32_t r0 = static_cast<int32_t>(max(begin - q0, int64_t{0}));
+    const int32_t r1 = static_cast<int32_t>(min(end - q0, static_cast<int64_t>(nr)));
+    if (!t.valid || !in_range(t.doc, 0, n, status)) continue;
+    for (int32_t rr = r0; rr < r1; ++rr) {
+      const int32_t r = r_base + rr;
+      const int32_t g = t.base + r * t.step;
+      if (in_range(g, 0, T, status)) out[rank < 0 ? r * S + t.j : t.j] = g;
+    }
   }
 }
 
-int grid_for(int64_t work, int threads, int per_sm) {
-  int64_t want = (work + threads - 1) / threads;
-  int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+// Blocks for `items` (slot tile, rank) work items: enough warps for
+// THD_ROUTE_MIN_ITEMS items each, at most THD_ROUTE_BLOCKS_PER_SM per SM.
+int grid_for_items(int64_t items) {
+  const int64_t warps = (items + THD_ROUTE_MIN_ITEMS - 1) / THD_ROUTE_MIN_ITEMS;
+  int64_t want = (warps + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
+  int64_t cap = static_cast<int64_t>(sm_count()) * THD_ROUTE_BLOCKS_PER_SM;
   if (want > cap) want = cap;
   if (want < 1) want = 1;
   return static_cast<int>(want);
@@ -213,11 +273,11 @@ thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t
   a.zc = zc ? *zc : thd_route_t{};
   a.cz = cz ? *cz : thd_route_t{};
   a.status = status;
-  size_t tables = static_cast<size_t>(2) * cp * (cp + 1) * sizeof(int32_t);
+  size_t tables = static_cast<size_t>(2 * cp + 3) * (cp + 1) * sizeof(int32_t);
   size_t cu_bytes = static_cast<size_t>(n + 1) * sizeof(int32_t);
   a.cu_in_smem = tables + cu_bytes <= static_cast<size_t>(kSmemBudget);
   size_t smem = tables + (a.cu_in_smem ? cu_bytes : 0);
-  int grid = grid_for(T, kRouteThreads, 2);
+  int grid = grid_for_items((static_cast<int64_t>(a.S) + 31) / 32 * cp);
   cudaError_t e;
   if (a.cu_in_smem) {
     if (dirs == (kZC | kCZ))
@@ -246,13 +306,12 @@ thd_status_t launch_partition(const int32_t* cu, int32_t n, int32_t T, int32_t c
   size_t cu_bytes = static_cast<size_t>(n + 1) * sizeof(int32_t);
   bool in_smem = cu_bytes <= static_cast<size_t>(kSmemBudget);
   int32_t S = T / cp;
-  int grid = grid_for(rank < 0 ? T : S, kRouteThreads, 2);
+  int grid = grid_for_items((static_cast<int64_t>(S) + 31) / 32 * (rank < 0 ? cp : 1));
   const CpMath m = make_cp_math(cp);
-  const FastDiv divS = make_fast_div(S > 0 ? S : 1);
   const cudaError_t e =
-      in_smem ? launch_pdl(partition_kernel<true>, grid, kRouteThreads, cu_bytes, s, cu, n, T, m, divS, S, rank, out,
+      in_smem ? launch_pdl(partition_kernel<true>, grid, kRouteThreads, cu_bytes, s, cu, n, T, m, S, rank, out,
                            status)
-              : launch_pdl(partition_kernel<false>, grid, kRouteThreads, 0, s, cu, n, T, m, divS, S, rank, out, status);
+              : launch_pdl(partition_kernel<false>, grid, kRouteThreads, 0, s, cu, n, T, m, S, rank, out, status);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

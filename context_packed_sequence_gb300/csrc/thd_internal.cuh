@@ -95,6 +95,31 @@ __device__ __forceinline__ int32_t block_check_cu(const int32_t* cu, int32_t n, 
   return THD_OK;
 }
 
+// Loads each thread keeps in flight while staging an array in shared memory.
+// Stores to shared memory cannot move above later global loads (a generic
+// pointer might alias shared memory), so a loop of one load and one store
+// per step would pay one memory round trip per step.
+constexpr int kStageBatch = 8;
+
+// Copy src[0, count) into shared memory, kStageBatch loads in flight per
+// thread before their stores (no barrier).
+__device__ __forceinline__ void stage_rows(const int32_t* src, int32_t count, int32_t* smem) {
+  const uint32_t uc = static_cast<uint32_t>(count), bd = blockDim.x;
+  for (uint32_t base = threadIdx.x; base < uc; base += kStageBatch * bd) {
+    int32_t v[kStageBatch];
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const uint32_t i = base + k * bd;
+      v[k] = i < uc ? src[i] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const uint32_t i = base + k * bd;
+      if (i < uc) smem[i] = v[k];
+    }
+  }
+}
+
 // Read the status word (one thread) while the block copies the n+1
 // boundaries into shared memory (when they fit), under one barrier.  Returns
 // true when the status word was already set; *view is the array to search.
@@ -103,22 +128,7 @@ __device__ __forceinline__ bool stage_cu_check_status(const int32_t* cu, int32_t
                                                       const int32_t** view) {
   __shared__ int32_t flag;
   if (threadIdx.x == 0) flag = status_load(st);
-  if (to_smem) {
-    // four independent loads in flight per thread before the stores
-    for (int32_t base = threadIdx.x; base <= n; base += 4 * blockDim.x) {
-      int32_t v[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int32_t i = base + k * static_cast<int32_t>(blockDim.x);
-        v[k] = i <= n ? cu[i] : 0;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int32_t i = base + k * static_cast<int32_t>(blockDim.x);
-        if (i <= n) smem[i] = v[k];
-      }
-    }
-  }
+  if (to_smem) stage_rows(cu, n + 1, smem);
   __syncthreads();
   *view = to_smem ? smem : cu;
   return flag != 0;
@@ -128,9 +138,59 @@ __device__ __forceinline__ bool stage_cu_check_status(const int32_t* cu, int32_t
 // the kernel should search.
 __device__ __forceinline__ const int32_t* stage_cu(const int32_t* cu, int32_t n, int32_t* smem, bool to_smem) {
   if (!to_smem) return cu;
-  for (int32_t i = threadIdx.x; i <= n; i += blockDim.x) smem[i] = cu[i];
+  stage_rows(cu, n + 1, smem);
   __syncthreads();
   return smem;
+}
+
+// Returned by stage_check_cu when the status word was already set.
+constexpr int32_t kStatusWasSet = -1;
+
+// Stage the n+1 boundaries in shared memory (when to_smem), validate them and
+// read the status word under a single barrier when nothing is wrong: every
+// thread loads a batch of boundary pairs (cu[i], cu[i+1]) at once, checks them
+// in registers (monotone, length divisible by mult >= 1) and keeps cu[i].
+// Returns kStatusWasSet when the status word was already non-zero, else the
+// first failing check in block_check_cu's order (cu[0] != 0, non-monotone,
+// not divisible, cu[n] != T), THD_OK when none.  Block-uniform.
+__device__ __forceinline__ int32_t stage_check_cu(const int32_t* cu, int32_t n, int32_t* smem, bool to_smem,
+                                                  const int32_t* st, int64_t T, int32_t mult) {
+  __shared__ int32_t flag;
+  if (threadIdx.x == 0) flag = status_load(st);
+  const bool pow2 = (mult & (mult - 1)) == 0;
+  const uint32_t um = static_cast<uint32_t>(mult), un = static_cast<uint32_t>(n), bd = blockDim.x;
+  int mono_bad = 0, div_bad = 0;
+  // the last boundary is loaded up front: a load after the loop's shared
+  // stores would cost one more round trip before the barrier
+  const int32_t last = (to_smem && threadIdx.x == 0) ? cu[n] : 0;
+  for (uint32_t base = threadIdx.x; base < un; base += kStageBatch * bd) {
+    int32_t lo[kStageBatch], hi[kStageBatch];
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const uint32_t i = base + k * bd;
+      lo[k] = i < un ? cu[i] : 0;
+      hi[k] = i < un ? cu[i + 1] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kStageBatch; ++k) {
+      const uint32_t i = base + k * bd;
+      if (i < un) {
+        // b - a of b >= a fits 32 unsigned bits whatever the values are
+        const uint32_t len = static_cast<uint32_t>(hi[k]) - static_cast<uint32_t>(lo[k]);
+        if (hi[k] < lo[k]) mono_bad = 1;
+        else if ((pow2 ? (len & (um - 1)) : (len % um)) != 0) div_bad = 1;
+        if (to_smem) smem[i] = lo[k];
+      }
+    }
+  }
+  if (to_smem && threadIdx.x == 0) smem[n] = last;
+  const int any_bad = __syncthreads_or(mono_bad | div_bad);
+  if (flag != 0) return kStatusWasSet;
+  const int32_t* v = to_smem ? smem : cu;
+  if (v[0] != 0) return THD_ERR_CU_NONZERO_START;
+  if (any_bad) return __syncthreads_or(mono_bad) ? THD_ERR_CU_NON_MONOTONE : THD_ERR_LEN_NOT_DIVISIBLE;
+  if (static_cast<int64_t>(v[n]) != T) return THD_ERR_TOTAL_MISMATCH;
+  return THD_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -204,120 +264,65 @@ __device__ __forceinline__ int32_t doc_from(const int32_t* cu, int32_t n, int32_
   return doc_in(cu, i, i + min(step - 1, n - i), x);
 }
 
-// The documents of a warp's 32 consecutive positions: one full search for
-// the lowest and the highest position (lanes 0 and 1 search, everyone gets
-// both answers), then a window search per lane, usually 0-2 steps.  lo_x and
-// hi_x must be the same in every lane, and every lane's x in [lo_x, hi_x].
-__device__ __forceinline__ int32_t warp_doc_of(const int32_t* cu, int32_t n, int32_t lo_x, int32_t hi_x,
-                                               int32_t x) {
-  const int lane = threadIdx.x & 31;
-  const int32_t found = doc_of(cu, n, lane == 0 ? lo_x : hi_x);
-  const int32_t i_lo = __shfl_sync(kFullMask, found, 0);
-  const int32_t i_hi = __shfl_sync(kFullMask, found, 1);
-  return doc_in(cu, i_lo, i_hi, x);
-}
-
-// Global row held by rank r at zigzag slot `slot`.  Rank-local document i
-// starts at slot cu[i]/cp (every padded length is a multiple of 2*cp), so the
-// document is found by searching cu for slot*cp.
-__device__ __forceinline__ int32_t zigzag_row(const int32_t* cu, int32_t n, CpMath m, int32_t r,
-                                              int32_t slot) {
-  int32_t i = doc_of(cu, n, slot * m.cp);
-  int32_t c0 = cu[i];
-  int32_t c = m.div2(cu[i + 1] - c0);
-  int32_t loc = slot - m.div(c0);
-  return loc < c ? c0 + r * c + loc : c0 + (2 * m.cp - 1 - r) * c + (loc - c);
-}
-
-// Zigzag buffer position (r*S + slot) of global row g.
-__device__ __forceinline__ int32_t zigzag_pos(const int32_t* cu, int32_t n, CpMath m, int32_t S,
-                                              int32_t g) {
-  int32_t i = doc_of(cu, n, g);
-  int32_t c0 = cu[i];
-  int32_t c = m.div2(cu[i + 1] - c0);
-  int32_t off = g - c0;
-  int32_t k = off / c;
-  int32_t j = off - k * c;
-  int32_t r = k < m.cp ? k : 2 * m.cp - 1 - k;
-  return r * S + m.div(c0) + (k < m.cp ? j : c + j);
-}
-
-// Number of zigzag rows of rank r with global index < X (0 <= X <= T):
-// earlier documents give cu[i]/cp rows, document i the clipped overlap of its
-// front chunk [r*c, (r+1)*c) and back chunk [(2cp-1-r)*c, (2cp-r)*c) with
-// [0, X - cu[i]).
-__device__ __forceinline__ int32_t zigzag_count_below(const int32_t* cu, int32_t n, CpMath m,
-                                                      int32_t S, int32_t T, int32_t r, int32_t X) {
-  if (X >= T) return S;
-  int32_t i = doc_of(cu, n, X);
-  int32_t c0 = cu[i];
-  int32_t c = m.div2(cu[i + 1] - c0);
-  int32_t off = X - c0;
-  int32_t a = min(max(off - r * c, 0), c);
-  int32_t b = min(max(off - (2 * m.cp - 1 - r) * c, 0), c);
-  return m.div(c0) + a + b;
-}
-
 // ---------------------------------------------------------------------------
-// walking the zigzag buffer in warp tiles
+// walking the zigzag layout in slot tiles
 // ---------------------------------------------------------------------------
 
-// A warp walks a contiguous range of zigzag positions u = r*S + j, 32 per
-// step, and keeps the document index of its lowest slot.  Within one rank
-// the slots only grow, so the next tile's documents are found by galloping
-// forward from there; a full search happens only at the start and where the
-// walk enters another rank.
-struct TileWalker {
-  int32_t doc;      // document of the lowest slot of the previous tile
-  int32_t rank;     // its rank (-1 before the first tile)
+// Every rank's zigzag shard has the same shape: document i fills local slots
+// [cu[i]/cp, cu[i+1]/cp) of each rank, its front chunk first, then its back
+// chunk.  Only the chunk indices depend on the rank, so the global row of
+// rank r at slot j is base_j + r*step_j with
+//   front (loc = j - cu[i]/cp < c):  base = cu[i] + loc,            step = +c
+//   back:                            base = cu[i] + (2cp-2)*c + loc, step = -c
+// (chunk r at offset loc, or chunk 2cp-1-r at offset loc-c).  A warp finds
+// the documents of 32 consecutive slots (a slot tile) once and serves every
+// rank from them.  Work items are (tile, rank) pairs, q = tile*cp + r; a warp
+// takes an equal contiguous share of them, so it visits few tiles and all or
+// most ranks of each.
+struct SlotTile {
+  int32_t j;           // this lane's slot, clamped to S-1 in the last tile
+  bool valid;          // the lane's slot is below S (clamped lanes must not store)
+  int32_t doc;         // document holding slot j
+  int32_t base, step;  // rank r's global row: base + r*step
 };
 
-struct TileRow {
-  int32_t u, r, j, g;
-  int32_t doc;  // the document holding g
-};
-
-// Lanes hold positions u (clamped to last, the walk's final position, for
-// the slot arithmetic; such lanes must not store).
-__device__ __forceinline__ TileRow tile_row(const int32_t* cu, int32_t n, CpMath m, int32_t S, FastDiv divS,
-                                            int32_t u, int32_t last, TileWalker& w) {
-  TileRow t;
-  t.u = u;
-  const int32_t uc = min(u, last);
-  t.r = divS.div(uc);
-  t.j = uc - t.r * S;
-  const int32_t r_first = __shfl_sync(kFullMask, t.r, 0), r_last = __shfl_sync(kFullMask, t.r, 31);
-  const int32_t x_lo = __shfl_sync(kFullMask, t.j, 0) * m.cp;
-  const int32_t x_hi = __shfl_sync(kFullMask, t.j, 31) * m.cp;
-  const int32_t x = t.j * m.cp;
-  int32_t i;
-  if (r_first == r_last) {
-    const int32_t i_lo = (w.rank == r_first) ? doc_from(cu, n, w.doc, x_lo) : doc_of(cu, n, x_lo);
-    const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
-    i = doc_in(cu, i_lo, i_hi, x);
-    w.doc = i_lo;
-    w.rank = r_first;
-  } else {  // the tile crosses into the next rank
-    i = doc_of(cu, n, x);
-    w.rank = -1;
-  }
+// Documents of the slots of tile `tile` (every lane of the warp calls it
+// with the same tile).  `wdoc` carries the document of the previous tile's
+// lowest slot (-1 before the first): tiles only move forward, so the next
+// one is found by galloping from there.  Slots are kept below S without
+// forming tile*32 + 31, which could pass INT32_MAX when S is near 2^31.
+__device__ __forceinline__ SlotTile slot_tile(const int32_t* cu, int32_t n, CpMath m, int32_t S,
+                                              int32_t tile, int32_t& wdoc) {
+  const int32_t lane = threadIdx.x & 31;
+  const int32_t j0 = tile * 32;  // tile < ceil(S/32), so j0 <= S - 1
+  const int32_t left = S - 1 - j0;
+  SlotTile t;
+  t.valid = lane <= left;
+  t.j = j0 + min(lane, left);
+  const int32_t x_lo = j0 * m.cp, x_hi = (j0 + min(31, left)) * m.cp;
+  const int32_t i_lo = wdoc < 0 ? doc_of(cu, n, x_lo) : doc_from(cu, n, wdoc, x_lo);
+  const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
+  wdoc = i_lo;
+  const int32_t i = doc_in(cu, i_lo, i_hi, t.j * m.cp);
   const int32_t c0 = cu[i];
   const int32_t c = m.div2(cu[i + 1] - c0);
   const int32_t loc = t.j - m.div(c0);
-  t.g = loc < c ? c0 + t.r * c + loc : c0 + (2 * m.cp - 1 - t.r) * c + (loc - c);
+  const bool front = loc < c;
   t.doc = i;
+  t.base = front ? c0 + loc : c0 + (2 * m.cp - 2) * c + loc;
+  t.step = front ? c : -c;
   return t;
 }
 
-// The warp's range of positions [begin, end) out of [0, total): equal shares,
-// whole tiles of 32.
-__device__ __forceinline__ void warp_range(int64_t total, int64_t* begin, int64_t* end) {
+// The warp's share [begin, end) of `total` work items: equal contiguous
+// shares, at least `min_per_warp` items each (later warps may get none).
+__device__ __forceinline__ void warp_items(int64_t total, int64_t min_per_warp, int64_t* begin, int64_t* end) {
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t tiles = (total + 31) / 32;
-  const int64_t per = (tiles + nwarps - 1) / nwarps;
-  *begin = min(total, warp * per * 32);
-  *end = min(total, (warp + 1) * per * 32);
+  int64_t per = (total + nwarps - 1) / nwarps;
+  if (per < min_per_warp) per = min_per_warp;
+  *begin = min(total, warp * per);
+  *end = min(total, *begin + per);
 }
 
 // ---------------------------------------------------------------------------
