@@ -1,5 +1,6 @@
-"""The largest packing the C ABI accepts: T = 2^31 - 16 rows (row indices are
-int32), cp = 8.
+"""The largest packings the C ABI accepts: T = 2^31 - 16 rows (row indices are
+int32) at cp = 8, and T = 2^31 - 2 at cp = 1, where a rank's slots run up to
+the top of the int32 range.
 
 One document of about 2^31 rows comes first (its chunks are ~1.3e8 rows, so
 the closed forms run at the top of the int32 range), then a thousand small
@@ -15,7 +16,10 @@ depend only on that document and where it starts):
   the rows they summarise;
 - a swap there and back returns the payload, whose rows carry their index;
 - labels of the small documents and of the large document's tail equal the
-  oracle's on that document.
+  oracle's on that document;
+- at cp = 1 the zigzag layout is the contiguous one (each document's two
+  chunks in order), so the partition and both routes are the identity and the
+  labels written in the zigzag layout equal the contiguous ones.
 
 About 100 GB of device memory at the peak."""
 
@@ -129,3 +133,67 @@ def test_labels_at_the_row_limit(big_gpu):
     head, head_valid = cu[1], cu_v[1]
     check(head - 64, head, 64 - (head - head_valid))
     assert int(valid.sum(dtype=torch.int64)) == cu_v[-1]
+
+
+T_MAX_CP1 = 2**31 - 2
+
+
+def _packing_cp1():
+    rng = np.random.default_rng(2**31 - 2)
+    tail = 2 * rng.integers(1, 257, size=500)              # 2 .. 512 rows, multiples of 2cp = 2
+    tail[rng.choice(500, size=10, replace=False)] = 0     # empty documents
+    head = T_MAX_CP1 - int(tail.sum())
+    lengths = [head] + tail.tolist()
+    valid = [head - 3] + [max(0, int(x) - int(rng.integers(0, 2))) for x in tail]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    cu_v = np.concatenate([[0], np.cumsum(valid)]).astype(np.int64)
+    assert cu[-1] == T_MAX_CP1 and head % 2 == 0
+    return cu.tolist(), cu_v.tolist()
+
+
+def _is_arange(t, chunk=2**28):
+    """t (int32, flat) equals 0, 1, ..., numel-1, compared a chunk at a time."""
+    n = t.numel()
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        if not torch.equal(t[lo:hi], torch.arange(lo, hi, dtype=torch.int32, device=t.device)):
+            return False
+    return True
+
+
+def test_cp1_partition_and_routes_at_the_row_limit(big_gpu):
+    cu, _ = _packing_cp1()
+    T = T_MAX_CP1
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    st = thd.new_status()
+    part = thd.partition_indices(cu_d, T, 1, -1, status=st)
+    thd.check_status(st)
+    assert _is_arange(part.reshape(-1))
+    part = thd.partition_indices(cu_d, T, 1, 0, status=st, out=part.reshape(-1))
+    thd.check_status(st)
+    assert _is_arange(part)
+    del part
+    fwd, bwd = thd.route_build_pair(cu_d, T, 1, status=st)
+    thd.check_status(st)
+    for r in (fwd, bwd):
+        assert _is_arange(r.src_of_dst)
+        assert _is_arange(r.send_rows.reshape(-1)) and _is_arange(r.recv_rows.reshape(-1))
+        assert r.input_split_sizes.tolist() == [[T]] and r.output_split_sizes.tolist() == [[T]]
+        assert bool(r.send_identity[0]) and bool(r.recv_identity[0])
+
+
+def test_cp1_zigzag_labels_at_the_row_limit(big_gpu):
+    cu, cu_v = _packing_cp1()
+    T = T_MAX_CP1
+    dev = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(37)
+    tokens = torch.randint(0, 151643, (T,), dtype=torch.int32, device="cuda", generator=g)
+    st = thd.new_status()
+    want = thd.roll_labels(tokens, dev(cu_v), dev(cu), 1, fill=-1, status=st)
+    got = thd.roll_labels_zigzag(tokens, dev(cu_v), dev(cu), 1, 1, fill=-1, status=st)
+    thd.check_status(st)
+    for a, b in zip(got, want):
+        assert a.shape == b.shape
+        for lo in range(0, T, 2**28):
+            assert torch.equal(a[..., lo:lo + 2**28], b[..., lo:lo + 2**28]), lo
