@@ -128,10 +128,11 @@ def copy_engine_digest():
     return h.hexdigest()
 
 
-def swap_traffic_record():
-    """dram bytes per swap launch from the committed ncu summary, or None when
-    the summary is missing or the copy kernel's sources changed since."""
-    path = os.path.join(ROOT, "profiles", "bulk_copy_swap_lognorm128k.md")
+def swap_traffic_record(workload: str):
+    """dram bytes per swap launch on this workload from the committed ncu
+    summary (profiles/bulk_copy_swap_<workload>.md), or None when the summary
+    is missing or the copy kernel's sources changed since."""
+    path = os.path.join(ROOT, "profiles", f"bulk_copy_swap_{workload}.md")
     try:
         text = open(path).read()
         digest = copy_engine_digest()
@@ -141,12 +142,13 @@ def swap_traffic_record():
     for line in text.splitlines():
         if line.startswith("- ") and ":" in line:
             k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("copy engine sha256") != digest:
+            fields[k.strip()] = v.strip()
+    recorded = next((v.strip("`") for k, v in fields.items() if k.startswith("copy engine sha256")), None)
+    if recorded != digest:
         return None
     try:
-        return int(fields["dram bytes per launch"])
-    except (KeyError, ValueError):
+        return int(fields["dram bytes per launch"].split()[0].replace(",", ""))
+    except (KeyError, ValueError, IndexError):
         return None
 
 
@@ -536,7 +538,7 @@ def run_thd(args, rank, world, local):
         e2e = run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes)
 
     peak, peak_kind = measured_peak()
-    traffic = swap_traffic_record()
+    traffic = swap_traffic_record(w.name)
     result = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -576,7 +578,7 @@ def run_thd(args, rank, world, local):
             "peak_kind": f"{peak_kind} copy bandwidth (read+write)",
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": traffic if w.name == "lognorm128k" else None,
+            "traffic": traffic,
             "algorithmic_bytes_per_launch": swap_bytes,
         },
         "gpu_launches": launches_per_step * n_ev * world,   # every rank's, like value
