@@ -535,7 +535,8 @@ def run_thd(args, rank, world, local):
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes)
+        e2e = run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes,
+                      steps=max(12, args.steps))
 
     peak, peak_kind = measured_peak()
     traffic = swap_traffic_record(w.name)
@@ -603,7 +604,9 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
     their own over `slots` device buffers, so uploads, downloads (the link is
     full duplex) and compute overlap; a slot is uploaded again only once its
     previous result has been read back.  The timed region spans the first
-    upload to the last download."""
+    upload to the last download; it runs as many steps as the device-timed
+    leg (at least 12), so the first upload and the last download, which
+    nothing overlaps, weigh the same in both."""
     x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_host.copy_(x)
     cu_host = cu_d.cpu().pin_memory()

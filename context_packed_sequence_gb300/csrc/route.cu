@@ -82,7 +82,7 @@ __device__ bool has_descent(const int32_t* cu, int32_t n, CpMath m, int32_t lo, 
   return false;
 }
 
-// Split sizes, offsets and identity flags of one direction (block 0 only).
+// Split sizes, offsets and identity flags of one direction (one block only).
 // n_zc[s][d] = cnt[s][d+1] - cnt[s][d] rows go from zigzag rank s to
 // contiguous rank d; the reverse direction transposes it.
 __device__ void write_small_arrays(const thd_route_t& r, bool z2c, const int32_t* cu, int32_t n, CpMath m,

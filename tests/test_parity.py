@@ -466,7 +466,7 @@ def test_roll_labels_parity(depth):
         assert got[2].cpu().tolist() == want[2]
 
 
-@pytest.mark.parametrize("cp,depth", [(1, 0), (2, 1), (4, 3), (8, 2)])
+@pytest.mark.parametrize("cp,depth", [(1, 0), (2, 1), (3, 1), (4, 3), (6, 0), (8, 2), (16, 3), (64, 1)])
 def test_roll_labels_zigzag_parity(cp, depth):
     rng = np.random.default_rng(70 + cp)
     for trial in range(8):
