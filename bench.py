@@ -602,11 +602,15 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
     builds both routes, runs the layers' swap pairs and copies the result back
     to pinned host memory.  Uploads and downloads run on two copy streams of
     their own over `slots` device buffers, so uploads, downloads (the link is
-    full duplex) and compute overlap; a slot is uploaded again only once its
-    previous result has been read back.  The timed region spans the first
-    upload to the last download; it runs as many steps as the device-timed
-    leg (at least 12), so the first upload and the last download, which
-    nothing overlaps, weigh the same in both."""
+    full duplex) and compute overlap.  Uploads are issued `slots - 1` steps
+    ahead; before refilling a slot the host waits for the download of the
+    slot's previous result (an event the download stream records).  The
+    waits stay on the host because a device-side wait there would close a
+    cycle of stream waits (compute on uploads, uploads on downloads,
+    downloads on compute), which cost about 0.6 ms per step on GB300.  The
+    timed region spans the first upload to the last download; it runs as
+    many steps as the device-timed leg (at least 12), so the first upload and
+    the last download, which nothing overlaps, weigh the same in both."""
     x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     x_host.copy_(x)
     cu_host = cu_d.cpu().pin_memory()
@@ -619,6 +623,7 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
     ks = torch.cuda.current_stream(device)
     ups, downs = torch.cuda.Stream(device), torch.cuda.Stream(device)
     cs = ups  # the link-only timings below
+    ahead = slots - 1
 
     def run(n):
         up = [torch.cuda.Event() for _ in range(n)]
@@ -626,14 +631,14 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
         freed = [torch.cuda.Event() for _ in range(n)]
 
         def upload(i):
+            if i >= slots:
+                freed[i - slots].synchronize()  # the slot's last result is read back
             with torch.cuda.stream(ups):
-                if i >= slots:
-                    ups.wait_event(freed[i - slots])  # the slot's last result is read back
                 xd[i % slots].copy_(x_host, non_blocking=True)
                 cud[i % slots].copy_(cu_host, non_blocking=True)
                 up[i].record(ups)
 
-        for i in range(min(slots, n)):
+        for i in range(min(ahead, n)):
             upload(i)
         for i in range(n):
             k = i % slots
@@ -647,8 +652,8 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
                 downs.wait_event(done[i])
                 out_host[k].copy_(xd[k], non_blocking=True)
                 freed[i].record(downs)
-            if i + slots < n:
-                upload(i + slots)
+            if i + ahead < n:
+                upload(i + ahead)
         ks.wait_stream(downs)
 
     run(2)
@@ -683,7 +688,8 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
             "h2d_bytes_per_step": int(x.numel() * x.element_size() + cu_d.numel() * 4),
             "d2h_bytes_per_step": int(x.numel() * x.element_size()),
             "ms_per_step": round(ms / steps, 3), "steps": steps,
-            "overlap": f"uploads and downloads on two copy streams, {slots} buffer slots, against compute",
+            "overlap": f"uploads ({ahead} steps ahead) and downloads on two copy streams, {slots} buffer slots, "
+                       "against compute; slot reuse waits on the host",
             "link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
