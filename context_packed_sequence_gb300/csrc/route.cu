@@ -25,16 +25,15 @@ namespace {
 
 constexpr int kRouteThreads = 512;
 constexpr int kSmemBudget = 48 * 1024;
-// Launch shape of the walking kernels: blocks per SM at most, and the least
-// number of (slot tile, rank) items a warp takes.
+// Launch shape of the walking kernels: at most this many blocks per SM (a
+// sweep on GB300 over 1-2 blocks per SM and 1-16 items per warp put one
+// block per SM, one warp per item, ahead by 1-2 us on 4096 documents and
+// level elsewhere).
 #ifndef THD_ROUTE_BLOCKS_PER_SM
 #define THD_ROUTE_BLOCKS_PER_SM 1
 #endif
-#ifndef THD_ROUTE_MIN_ITEMS
-#define THD_ROUTE_MIN_ITEMS 1
-#endif
-// Ranks of one slot tile handled together by a lane (independent chains of
-// arithmetic, table loads and stores that overlap).
+// Unrolling of a lane's loop over the ranks of a slot tile (1-8 timed the
+// same on GB300; 1 keeps the kernels at 32 registers).
 #ifndef THD_ROUTE_UNROLL
 #define THD_ROUTE_UNROLL 1
 #endif
@@ -178,7 +177,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   //   send buffer, with value g - d*S.
   const int64_t tiles = (static_cast<int64_t>(S) + 31) / 32;
   int64_t begin, end;
-  warp_items(tiles * cp, THD_ROUTE_MIN_ITEMS, &begin, &end);
+  warp_items(tiles * cp, 1, &begin, &end);
   if (begin >= end) return;
   const FastDiv divS = a.divS;
   int32_t wdoc = -1;
@@ -229,7 +228,7 @@ partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, CpMath m, int32_t S,
   const int32_t r_base = rank < 0 ? 0 : rank;
   const int64_t tiles = (static_cast<int64_t>(S) + 31) / 32;
   int64_t begin, end;
-  warp_items(tiles * nr, THD_ROUTE_MIN_ITEMS, &begin, &end);
+  warp_items(tiles * nr, 1, &begin, &end);
   if (begin >= end) return;
   int32_t wdoc = -1;
   const int32_t t_last = static_cast<int32_t>((end - 1) / nr);
@@ -247,11 +246,10 @@ partition_kernel(const int32_t* cu_g, int32_t n, int32_t T, CpMath m, int32_t S,
   }
 }
 
-// Blocks for `items` (slot tile, rank) work items: enough warps for
-// THD_ROUTE_MIN_ITEMS items each, at most THD_ROUTE_BLOCKS_PER_SM per SM.
+// Blocks for `items` (slot tile, rank) work items: a warp per item, at most
+// THD_ROUTE_BLOCKS_PER_SM blocks per SM.
 int grid_for_items(int64_t items) {
-  const int64_t warps = (items + THD_ROUTE_MIN_ITEMS - 1) / THD_ROUTE_MIN_ITEMS;
-  int64_t want = (warps + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
+  int64_t want = (items + kRouteThreads / 32 - 1) / (kRouteThreads / 32);
   int64_t cap = static_cast<int64_t>(sm_count()) * THD_ROUTE_BLOCKS_PER_SM;
   if (want > cap) want = cap;
   if (want < 1) want = 1;
