@@ -667,3 +667,60 @@ def test_full_size_pipeline():
     idx = torch.tensor(oracle.partition_indices(cu_o, len(tok_o), w.cp, -1), device="cuda").long()
     assert torch.equal(zl, labels[:, idx]) and torch.equal(zm, lmask[:, idx]) and torch.equal(zv, valid[idx])
     _full_size_swap_check(cu_o, w.cp, w.hidden, w.seed, sample=2048)
+
+
+def test_pipeline_fuzz():
+    """Random raw batches through the whole path, every stage against the
+    oracle: packing (EOD density, trailing raw pad, extra tokens), labels and
+    MTP targets in both layouts, the partition of every rank, both routes in
+    one launch, then the payload swapped there and back for several row
+    widths (4, 16, 48, 512 and 4096 bytes: the unit, run and bulk engines)
+    and through the three separate steps."""
+    rng = np.random.default_rng(2024)
+    E = 7
+    for trial in range(10):
+        cp = int(rng.choice([1, 2, 3, 4, 8]))
+        B, S = int(rng.integers(1, 7)), int(rng.integers(1, 2500))
+        raw = rng.integers(10, 1000, size=(B, S)).astype(np.int32)
+        raw[rng.random((B, S)) < float(rng.choice([0.0005, 0.003, 0.03]))] = E
+        trim = trial % 3 == 1
+        if trim:
+            raw[rng.integers(0, B), S - S // 3:] = 0
+        extra = rng.integers(2000, 3000, size=B).astype(np.int32) if trial % 2 else None
+        tok_o, cu_v_o, cu_o, *nx = oracle.pack_docs(raw.tolist(), E, 2 * cp, pad_id=0,
+                                                    raw_pad_id=0 if trim else None,
+                                                    row_next=None if extra is None else extra.tolist())
+        nxt_o = nx[0] if nx else None
+        got = thd.pack_docs(torch.from_numpy(raw).cuda(), E, 2 * cp, pad_id=0, raw_pad_id=0 if trim else None,
+                            row_next=None if extra is None else torch.from_numpy(extra).cuda())
+        tok, cu_v, cu = got[:3]
+        nt, hn = (got[3], got[4]) if extra is not None else (None, None)
+        assert tok.cpu().tolist() == tok_o and cu_v.cpu().tolist() == cu_v_o and cu.cpu().tolist() == cu_o
+        T = len(tok_o)
+        depth = int(rng.integers(0, 4))
+        st = thd.new_status()
+        lab = thd.roll_labels(tok, cu_v, cu, depth, -1, status=st, next_token=nt, has_next=hn)
+        lab_z = thd.roll_labels_zigzag(tok, cu_v, cu, cp, depth, -1, status=st, next_token=nt, has_next=hn)
+        part = thd.partition_indices(cu, T, cp, -1, status=st)
+        fwd, bwd = thd.route_build_pair(cu, T, cp, status=st)
+        thd.check_status(st)
+        assert [g.cpu().tolist() for g in lab] == [list(v) for v in
+                                                   oracle.roll_labels(tok_o, cu_v_o, cu_o, depth, fill=-1,
+                                                                      doc_next=nxt_o)]
+        assert [g.cpu().tolist() for g in lab_z] == [list(v) for v in
+                                                     oracle.roll_labels_zigzag(tok_o, cu_v_o, cu_o, cp, depth,
+                                                                               fill=-1, doc_next=nxt_o)]
+        assert part.reshape(-1).cpu().tolist() == oracle.partition_indices(cu_o, T, cp, -1)
+        want = [oracle.build_route(cu_o, T, cp, d) for d in (Z2C, C2Z)]
+        _assert_route(fwd, want[Z2C])
+        _assert_route(bwd, want[C2Z])
+        for row_bytes in (4, 16, 48, 512, 4096):
+            x = torch.from_numpy(rng.integers(0, 256, size=(T, row_bytes), dtype=np.uint8)).cuda()
+            y = thd.swap(x, fwd, status=st)
+            y3 = thd.scatter(thd.a2a_local(thd.pack(x, fwd, status=st), fwd, status=st), fwd, status=st)
+            z = thd.swap(y, bwd, status=st)
+            thd.check_status(st)
+            _, _, y_o = oracle.apply_route(x.cpu().numpy(), want[Z2C])
+            assert np.array_equal(y.cpu().numpy(), y_o), (trial, cp, T, row_bytes)
+            assert torch.equal(y3, y), (trial, cp, T, row_bytes)
+            assert torch.equal(z, x), (trial, cp, T, row_bytes)
