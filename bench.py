@@ -470,18 +470,21 @@ def run_thd(args, rank, world, local):
     uly = None
     if row_bytes % cp == 0 and T % cp == 0:
         def uly_time(direction, src, dst):
+            """Per-launch time of 20 launches back to back (as the swaps run
+            inside a step), median of 10: each direction rewrites the same
+            output, head -> sequence of y giving back x."""
             ts = []
-            for it in range(25):
-                if it == 0 or it % 5 == 0:
-                    torch.cuda._sleep(200_000)
+            for it in range(12):
+                torch.cuda._sleep(200_000)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                lib.thd_ulysses_swap(src.data_ptr(), dst.data_ptr(), T, cp, row_bytes, direction, status.data_ptr(),
-                                     sp)
+                for _ in range(20):
+                    lib.thd_ulysses_swap(src.data_ptr(), dst.data_ptr(), T, cp, row_bytes, direction,
+                                         status.data_ptr(), sp)
                 b.record(stream)
                 torch.cuda.synchronize(device)
-                if it >= 5:
-                    ts.append(a.elapsed_time(b) * 1e3)
+                if it >= 2:
+                    ts.append(a.elapsed_time(b) * 1e3 / 20)
             return statistics.median(ts)
 
         peak_gbs, _ = measured_peak()
@@ -498,6 +501,7 @@ def run_thd(args, rank, world, local):
                   else "tile transpose or row engine, by tokens per tile" if tiled and piece < 1024
                   else "row engine")
         uly = {"piece_bytes": piece, "engine": engine, "seq_to_head_us": round(to_head, 2),
+               "method": "20 launches back to back per direction, per launch, median of 10",
                "head_to_seq_us": round(to_seq, 2),
                "gbs": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3, 1),
                "frac_of_measured": round(swap_bytes / ((to_head + to_seq) / 2) / 1e3 / peak_gbs, 4)}
