@@ -13,12 +13,16 @@
 //      1. stats: per chunk, its document ends (EODs, and the row's last valid
 //         token), its first and last end, and the padded lengths of the
 //         documents that both start and end inside it;
-//      2. emit: every block scans the statistics of all chunks (a max-scan
-//         carries each row's last end into the next chunk, which fixes the
-//         length of the document open at a chunk boundary; sum-scans give
-//         each chunk's first document index and output offset), then writes
-//         its tokens, padding and boundaries.
-//    Scratch: one int64 per row and four per chunk.
+//      2. scan: over the statistics of all chunks in order, a max-scan
+//         carries each row's last end into the next chunk (which fixes the
+//         length of the document open at a chunk boundary) and sum-scans give
+//         each chunk's first document index and output offset; a sum over the
+//         rows gives each row's unpadded offset; the totals go to `counts`,
+//         checked against the capacities.  Up to 512 chunks (about 1M raw
+//         tokens) every emit block does this for itself; beyond that one
+//         block does it first and stores every chunk's carries;
+//      3. emit: every chunk writes its tokens, padding and boundaries.
+//    Scratch: two int64 per row, seven per chunk and two totals.
 //  * per row (thd_pack_docs_noalloc, whose scratch is a fixed array of four
 //    int64 per row): the same two phases with one block per raw row.
 #include "thd_internal.cuh"
@@ -270,24 +274,14 @@ pack_chunk_stats_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int6
   }
 }
 
-__global__ void __launch_bounds__(kChunkThreads)
-pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64_t* ve_arr, int32_t align,
-                       int32_t pad_id, const int64_t* stats, const int32_t* row_next, int32_t* tokens,
-                       int64_t tok_cap, int32_t* cu_v, int32_t* cu, int32_t* next_tok, uint8_t* has_next,
-                       int64_t docs_cap, int64_t* counts, int32_t* status) {
-  __shared__ int64_t tmp[32];
-  __shared__ int64_t carry[4];  // last end before this chunk in its row, first doc index, output offset
-  pdl_wait_then_release();
-  if (block_status_set(status)) return;
-  const int64_t b = blockIdx.y, c = blockIdx.x, me = b * g.per_row + c;
+// The block walks every chunk's statistics in order: a max-scan carries
+// each row's last end into the next chunk, sum-scans give every chunk's first
+// document index and output offset.  Chunk z's three carries go to
+// carry_out[z * 3 ...] when carry_out is set, else only chunk `mine`'s to
+// mine_out[0..2]; totals_out gets {documents, padded tokens}.
+__device__ void scan_chunks(const ChunkGeom& g, int32_t align, const int64_t* stats, int64_t* carry_out,
+                            int64_t mine, int64_t* mine_out, int64_t* totals_out, int64_t* tmp) {
   const int64_t key_span = g.S + 2;  // key = row * key_span + (last end + 1)
-
-  // valid tokens of the rows before this one (the global unpadded offset)
-  int64_t v_before = 0;
-  for (int64_t r = threadIdx.x; r < b; r += blockDim.x) v_before += ve_arr ? ve_arr[r] : g.S;
-  v_before = block_sum(v_before, tmp);
-
-  // every chunk's documents and padded length, in order, 256 chunks a pass
   int64_t key_carry = -1, docs_carry = 0, pad_carry = 0;
   for (int64_t base = 0; base < g.nc; base += blockDim.x) {
     const int64_t z = base + threadIdx.x;
@@ -310,29 +304,116 @@ pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64
     int64_t pass_docs, pass_pad;
     const int64_t docs_before = block_exclusive_scan(n_end, OpSum(), static_cast<int64_t>(0), tmp, &pass_docs);
     const int64_t pad_before = block_exclusive_scan(pad_len, OpSum(), static_cast<int64_t>(0), tmp, &pass_pad);
-    if (z == me) {
-      carry[0] = prev_end;
-      carry[1] = docs_carry + docs_before;
-      carry[2] = pad_carry + pad_before;
+    int64_t* out = carry_out ? (z < g.nc ? carry_out + z * 3 : nullptr) : (z == mine ? mine_out : nullptr);
+    if (out) {
+      out[0] = prev_end;
+      out[1] = docs_carry + docs_before;
+      out[2] = pad_carry + pad_before;
     }
     key_carry = max(key_carry, pass_key);
     docs_carry += pass_docs;
     pad_carry += pass_pad;
   }
-  __syncthreads();
-  const int64_t d_all = docs_carry, t_all = pad_carry;
-  const bool over = d_all + 1 > docs_cap || t_all > tok_cap || t_all > INT32_MAX;
-  if (me == 0 && threadIdx.x == 0) {
-    counts[0] = d_all;
-    counts[1] = t_all;
-    if (over) {
-      status_set(status, THD_ERR_CAPACITY);
-    } else {
-      cu[0] = 0;
-      cu_v[0] = 0;
+  if (threadIdx.x == 0) {
+    totals_out[0] = docs_carry;
+    totals_out[1] = pad_carry;
+  }
+}
+
+// Sizes, counts and the first boundaries once the totals are known: counts
+// always, then THD_ERR_CAPACITY when the outputs are too small (nothing is
+// emitted), else cu[0] = cu_v[0] = 0.  One thread.
+__device__ void publish_totals(int64_t d_all, int64_t t_all, int64_t tok_cap, int64_t docs_cap, int32_t* cu_v,
+                               int32_t* cu, int64_t* counts, int32_t* status) {
+  counts[0] = d_all;
+  counts[1] = t_all;
+  if (d_all + 1 > docs_cap || t_all > tok_cap || t_all > INT32_MAX) {
+    status_set(status, THD_ERR_CAPACITY);
+  } else {
+    cu[0] = 0;
+    cu_v[0] = 0;
+  }
+}
+
+// Up to this many chunks every emit block scans the statistics itself (two
+// launches); beyond it one block scans them first (three launches), since
+// the self-scan costs every block a pass over all chunks.
+constexpr int64_t kSelfScanChunks = 512;
+
+// One block over all chunks (more than kSelfScanChunks): every chunk's carries,
+// every row's unpadded offset (vbefore, when the rows are trimmed) and the
+// totals.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+pack_chunk_scan_kernel(ChunkGeom g, const int64_t* ve_arr, int32_t align, const int64_t* stats, int64_t* carry,
+                       int64_t* vbefore, int64_t* totals, int64_t tok_cap, int64_t docs_cap, int32_t* cu_v,
+                       int32_t* cu, int64_t* counts, int32_t* status) {
+  __shared__ int64_t tmp[32];
+  __shared__ int64_t tot[2];
+  pdl_wait_then_release();
+  if (block_status_set(status)) return;
+  scan_chunks(g, align, stats, carry, -1, nullptr, tot, tmp);
+  if (ve_arr) {
+    int64_t v_carry = 0;
+    for (int64_t base = 0; base < g.B; base += blockDim.x) {
+      const int64_t r = base + threadIdx.x;
+      const int64_t v = r < g.B ? ve_arr[r] : 0;
+      int64_t pass_v;
+      const int64_t v_before = block_exclusive_scan(v, OpSum(), static_cast<int64_t>(0), tmp, &pass_v);
+      if (r < g.B) vbefore[r] = v_carry + v_before;
+      v_carry += pass_v;
     }
   }
-  if (over) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    totals[0] = tot[0];
+    totals[1] = tot[1];
+    publish_totals(tot[0], tot[1], tok_cap, docs_cap, cu_v, cu, counts, status);
+  }
+}
+
+__global__ void __launch_bounds__(kChunkThreads)
+pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64_t* ve_arr, int32_t align,
+                       int32_t pad_id, const int64_t* stats, const int64_t* carry, const int64_t* vbefore,
+                       const int64_t* totals, const int32_t* row_next, int32_t* tokens, int64_t tok_cap,
+                       int32_t* cu_v, int32_t* cu, int32_t* next_tok, uint8_t* has_next, int64_t docs_cap,
+                       int64_t* counts, int32_t* status) {
+  __shared__ int64_t tmp[32];
+  __shared__ int64_t mine[3], tot[2];
+  pdl_wait_then_release();
+  // (with a separate scan, that kernel has set the status word when the
+  // capacities are too small)
+  if (block_status_set(status)) return;
+  const int64_t b = blockIdx.y, c = blockIdx.x, me = b * g.per_row + c;
+  int64_t d_all, t_all, v_before, carry_end, carry_doc, carry_out;
+  if (carry) {
+    d_all = totals[0];
+    t_all = totals[1];
+    v_before = ve_arr ? vbefore[b] : b * g.S;
+    carry_end = carry[me * 3 + 0];
+    carry_doc = carry[me * 3 + 1];
+    carry_out = carry[me * 3 + 2];
+  } else {
+    // few chunks: scan them all here, and the rows before this one
+    int64_t vb = 0;
+    if (ve_arr) {
+      for (int64_t r = threadIdx.x; r < b; r += blockDim.x) vb += ve_arr[r];
+      vb = block_sum(vb, tmp);
+    } else {
+      vb = b * g.S;
+    }
+    v_before = vb;
+    scan_chunks(g, align, stats, nullptr, me, mine, tot, tmp);
+    __syncthreads();
+    d_all = tot[0];
+    t_all = tot[1];
+    carry_end = mine[0];
+    carry_doc = mine[1];
+    carry_out = mine[2];
+    if (me == 0 && threadIdx.x == 0) publish_totals(d_all, t_all, tok_cap, docs_cap, cu_v, cu, counts, status);
+  }
+  if (d_all + 1 > docs_cap || t_all > tok_cap || t_all > INT32_MAX) return;  // reported once, above
 
   const int32_t* row = raw + b * g.S;
   const int64_t ve = ve_arr ? ve_arr[b] : g.S;
@@ -345,7 +426,7 @@ pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64
   }
   int64_t unused;
   int64_t first_prev = block_exclusive_scan(my_last, OpMax(), static_cast<int64_t>(-1), tmp, &unused);
-  first_prev = max(first_prev, carry[0]);
+  first_prev = max(first_prev, carry_end);
   int64_t cnt = 0, psum = 0;
   {
     int64_t pe = first_prev;
@@ -361,8 +442,8 @@ pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64
   const int64_t cnt_before = block_exclusive_scan(cnt, OpSum(), static_cast<int64_t>(0), tmp, &unused);
   const int64_t psum_before = block_exclusive_scan(psum, OpSum(), static_cast<int64_t>(0), tmp, &unused);
   int64_t pe = first_prev;
-  int64_t doc = carry[1] + cnt_before;  // document the next token belongs to
-  int64_t out = carry[2] + psum_before; // that document's first output row
+  int64_t doc = carry_doc + cnt_before;  // document the next token belongs to
+  int64_t out = carry_out + psum_before; // that document's first output row
   for (int it = 0; it < kChunkItems; ++it) {
     const int64_t t = t0 + it;
     if (t >= hi) break;
@@ -424,9 +505,12 @@ thd_status_t launch_pack_docs_rows(const int32_t* raw, int32_t B, int64_t S, int
 
 namespace thd {
 
+// int64 words: row valid ends [B], chunk statistics [nc][4], chunk carries
+// [nc][3], row offsets [B], totals [2]
 size_t pack_docs_chunked_workspace(int32_t B, int64_t S) {
   const int64_t per_row = (S + kChunk - 1) / kChunk;
-  return static_cast<size_t>(B) * sizeof(int64_t) + static_cast<size_t>(B) * per_row * 4 * sizeof(int64_t);
+  const int64_t nc = static_cast<int64_t>(B) * per_row;
+  return static_cast<size_t>(2 * static_cast<int64_t>(B) + 7 * nc + 2) * sizeof(int64_t);
 }
 
 thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t trim,
@@ -452,6 +536,9 @@ thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t 
   g.nc = static_cast<int64_t>(B) * g.per_row;
   int64_t* ve = trim ? ws : nullptr;
   int64_t* stats = ws + B;
+  int64_t* carry = stats + 4 * g.nc;
+  int64_t* vbefore = carry + 3 * g.nc;
+  int64_t* totals = vbefore + B;
   if (trim) {
     if ((e = launch_pdl(pack_row_ends_kernel, B, kPackThreads, 0, s, raw, S, raw_pad, ws, status)) != cudaSuccess) {
       record_cuda_error(e);
@@ -464,9 +551,19 @@ thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t 
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
+  const bool self_scan = g.nc <= kSelfScanChunks;
+  if (!self_scan &&
+      (e = launch_pdl(pack_chunk_scan_kernel, 1, kScanThreads, 0, s, g, static_cast<const int64_t*>(ve), align,
+                      static_cast<const int64_t*>(stats), carry, vbefore, totals, tok_cap, docs_cap, cu_v, cu, counts,
+                      status)) != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
   if ((e = launch_pdl(pack_chunk_emit_kernel, grid, kChunkThreads, 0, s, raw, g, eod,
-                      static_cast<const int64_t*>(ve), align, pad_id, static_cast<const int64_t*>(stats), row_next,
-                      tokens, tok_cap, cu_v, cu, next_tok, has_next, docs_cap, counts, status)) != cudaSuccess) {
+                      static_cast<const int64_t*>(ve), align, pad_id, static_cast<const int64_t*>(stats),
+                      static_cast<const int64_t*>(self_scan ? nullptr : carry), static_cast<const int64_t*>(vbefore),
+                      static_cast<const int64_t*>(totals), row_next, tokens, tok_cap, cu_v, cu, next_tok, has_next,
+                      docs_cap, counts, status)) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }

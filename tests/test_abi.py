@@ -149,5 +149,6 @@ def test_host_checks_return_before_any_launch(lib):
                              64, fake, None) == L.ERR_INVALID_ARG   # align 0
     assert lib.thd_pack_docs(fake, 2, 8, 99, 0, 0, 4, 0, fake, fake, 16, fake, fake, None, None, 4, fake, fake,
                              64, fake, None) == L.ERR_INVALID_ARG   # row_next without has_next
-    assert lib.thd_pack_docs_workspace_bytes(8, 4096) == 8 * 8 + 8 * 2 * 32
+    # two int64 per row, seven per 2048-token chunk (8 rows x 2 chunks), two totals
+    assert lib.thd_pack_docs_workspace_bytes(8, 4096) == 8 * (2 * 8 + 7 * 16 + 2)
     assert lib.thd_status_clear(None, None) == L.ERR_INVALID_ARG

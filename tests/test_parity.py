@@ -593,6 +593,34 @@ def test_pack_docs_long_rows_with_trailing_pad():
     assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
 
 
+def test_pack_docs_many_chunks_and_rows():
+    """More than 1024 chunks and more than 1024 rows: the scan over the chunk
+    statistics and over the rows' valid lengths runs in several passes.
+    Two rows of just over 2^20 tokens (1026 chunks of 2048), then 1500 short
+    rows with trailing pads trimmed and extra tokens."""
+    rng = np.random.default_rng(77)
+    B, S = 2, 2**20 + 123
+    raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+    raw[rng.random((B, S)) < 1 / 3000] = 7
+    raw[0, 2048 * 300] = 7                        # an EOD at a chunk start
+    want = oracle.pack_docs(raw.tolist(), 7, 8, pad_id=3)
+    got = thd.pack_docs(torch.from_numpy(raw).cuda(), 7, 8, pad_id=3)
+    assert [g.cpu().tolist() for g in got] == [list(w) for w in want]
+
+    B, S = 1500, 37
+    raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+    raw[rng.random((B, S)) < 0.1] = 7
+    for b in range(0, B, 3):
+        raw[b, int(rng.integers(0, S + 1)):] = 0   # trailing pad (some rows all pad)
+    extra = rng.integers(100, 200, size=B).astype(np.int32)
+    want = oracle.pack_docs(raw.tolist(), 7, 4, pad_id=0, raw_pad_id=0, row_next=extra.tolist())
+    tok, cu_v, cu, nt, hn = thd.pack_docs(torch.from_numpy(raw).cuda(), 7, 4, pad_id=0, raw_pad_id=0,
+                                          row_next=torch.from_numpy(extra).cuda())
+    assert tok.cpu().tolist() == want[0] and cu_v.cpu().tolist() == want[1] and cu.cpu().tolist() == want[2]
+    assert hn.cpu().tolist() == [int(v is not None) for v in want[3]]
+    assert [v for v, h in zip(nt.cpu().tolist(), hn.cpu().tolist()) if h] == [v for v in want[3] if v is not None]
+
+
 # --------------------------------------------------------------------------
 # the full-size workloads, in the launch configuration the benchmark times
 # --------------------------------------------------------------------------
