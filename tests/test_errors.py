@@ -196,6 +196,22 @@ def test_pack_docs_reports_a_too_small_output(tokens_capacity, ok):
     assert (tok.cpu().tolist(), cu_v.cpu().tolist(), cu.cpu().tolist()) == tuple(want)
 
 
+def test_pack_docs_capacity_with_many_chunks():
+    """Above 512 chunks the capacity check runs in the separate scan kernel:
+    two rows of just over 2^20 tokens (1026 chunks) need T output tokens;
+    room for T - 1 raises THD_ERR_CAPACITY, room for exactly T packs."""
+    rng = np.random.default_rng(91)
+    raw = rng.integers(1, 50, size=(2, 2**20 + 123)).astype(np.int32)
+    raw[rng.random(raw.shape) < 1 / 2500] = 99
+    T = len(oracle.pack_docs(raw.tolist(), 99, 16)[0])
+    x = torch.from_numpy(raw).cuda()
+    with pytest.raises(thd.ThdError) as e:
+        thd.pack_docs(x, 99, 16, tokens_capacity=T - 1)
+    assert e.value.kind == "capacity"
+    tok, cu_v, cu = thd.pack_docs(x, 99, 16, tokens_capacity=T)
+    assert tok.numel() == T and int(cu[-1]) == T
+
+
 @pytest.mark.skipif(os.environ.get("THD_CHECKED") != "1", reason="the debug request is in the checked build only")
 @pytest.mark.parametrize("width", [1024, 8])
 def test_bulk_wait_that_runs_out_reports_timeout(width):
