@@ -57,7 +57,12 @@ __device__ __forceinline__ void write_targets(const int32_t* __restrict__ tokens
   }
 }
 
-template <bool SMEM_CU>
+// Positions per lane: a lane writes each depth's four labels with one
+// 16-byte store and its four masks with one 4-byte store (VEC: T a multiple
+// of 4, labels 16-byte and masks 4-byte aligned), else one position at a time.
+constexpr int kPerLane = 4;
+
+template <bool SMEM_CU, bool VEC>
 __global__ void __launch_bounds__(kLabelThreads)
 roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
                    int32_t n, int32_t T, int32_t depth, int32_t fill, NextTokens next, int32_t* __restrict__ labels,
@@ -86,30 +91,80 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
   }
   if (T == 0) return;
 
-  // Each warp walks an equal contiguous range of positions, 32 per step,
-  // following the document of its lowest position forward (galloping search).
+  // Each warp walks an equal contiguous range of positions, 128 per step
+  // (four consecutive ones per lane), following the document of its lowest
+  // position forward (galloping search).  Steps start at multiples of 128, so
+  // p + 3 stays within int32 for every T below 2^31.
+  constexpr int kStep = 32 * kPerLane;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t tiles = (static_cast<int64_t>(T) + 31) / 32;
+  const int64_t tiles = (static_cast<int64_t>(T) + kStep - 1) / kStep;
   const int64_t per = (tiles + nwarps - 1) / nwarps;
-  const int64_t begin = min(static_cast<int64_t>(T), warp * per * 32);
-  const int64_t end = min(static_cast<int64_t>(T), (warp + 1) * per * 32);
+  const int64_t begin = min(static_cast<int64_t>(T), warp * per * kStep);
+  const int64_t end = min(static_cast<int64_t>(T), (warp + 1) * per * kStep);
   const int32_t lane = threadIdx.x & 31;
+  const int32_t last = static_cast<int32_t>(end) - 1;
   int32_t doc = -1;
-  for (int64_t tile0 = begin; tile0 < end; tile0 += 32) {
-    const int32_t p = static_cast<int32_t>(tile0) + lane;
-    const int32_t pc = min(p, static_cast<int32_t>(end) - 1);
+  for (int64_t tile0 = begin; tile0 < end; tile0 += kStep) {
+    const int32_t p0 = static_cast<int32_t>(tile0) + kPerLane * lane;
     const int32_t x_lo = static_cast<int32_t>(tile0);
-    const int32_t x_hi = __shfl_sync(kFullMask, pc, 31);
+    const int32_t x_hi = __shfl_sync(kFullMask, min(p0 + kPerLane - 1, last), 31);
     const int32_t i_lo = doc < 0 ? doc_of(cu, n, x_lo) : doc_from(cu, n, doc, x_lo);
     const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
-    const int32_t i = doc_in(cu, i_lo, i_hi, pc);
+    int32_t i = doc_in(cu, i_lo, i_hi, min(p0, last));
     doc = i_lo;
-    if (p < end && in_range(i, 0, n, status)) {
-      const int32_t e = cu[i] + (cu_v[i + 1] - cu_v[i]);  // end of the document's valid tokens
-      if (!in_range(e, 0, static_cast<int64_t>(T) + 1, status)) continue;  // token reads stay below e
-      valid[p] = p < e ? 1 : 0;
-      write_targets(tokens, next, i, p, p, e, depth, fill, T, labels, lmask);
+    if (p0 > last || !in_range(i, 0, n, status)) continue;
+    // each position's document, valid end and continuation
+    int32_t di[kPerLane], ei[kPerLane];
+    bool full = p0 + kPerLane - 1 <= last, bad = false;
+    uint32_t vbits = 0;
+#pragma unroll
+    for (int t = 0; t < kPerLane; ++t) {
+      const int32_t q = p0 + t;
+      if (q > last) {
+        di[t] = i, ei[t] = 0;
+        continue;
+      }
+      while (cu[i + 1] <= q) ++i;  // q < T = cu[n]: stops before i = n
+      di[t] = i;
+      ei[t] = cu[i] + (cu_v[i + 1] - cu_v[i]);  // end of the document's valid tokens
+      bad |= !in_range(ei[t], 0, static_cast<int64_t>(T) + 1, status);  // token reads stay below e
+      vbits |= (q < ei[t] ? 1u : 0u) << (8 * t);
+    }
+    if (bad) continue;
+    if (VEC && full) {
+      *reinterpret_cast<uint32_t*>(valid + p0) = vbits;
+    } else {
+      for (int t = 0; t < kPerLane && p0 + t <= last; ++t) valid[p0 + t] = static_cast<uint8_t>(vbits >> (8 * t));
+    }
+    for (int32_t k = 0; k <= depth; ++k) {
+      int32_t v[kPerLane];
+      uint32_t mbits = 0;
+#pragma unroll
+      for (int t = 0; t < kPerLane; ++t) {
+        const int32_t q = p0 + t;
+        v[t] = fill;
+        if (q > last) continue;
+        // depth k reads tokens[q+1+k] while k < room (no sum passes e)
+        const int32_t room = ei[t] - q - 1;
+        if (k < room) {
+          v[t] = __ldg(tokens + q + 1 + k);
+          mbits |= 1u << (8 * t);
+        } else if (k == room && next.has != nullptr && next.has[di[t]] != 0) {
+          v[t] = next.tok[di[t]];
+          mbits |= 1u << (8 * t);
+        }
+      }
+      const int64_t o = static_cast<int64_t>(k) * T + p0;
+      if (VEC && full) {
+        *reinterpret_cast<int4*>(labels + o) = make_int4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<uint32_t*>(lmask + o) = mbits;
+      } else {
+        for (int t = 0; t < kPerLane && p0 + t <= last; ++t) {
+          labels[o + t] = v[t];
+          lmask[o + t] = static_cast<uint8_t>(mbits >> (8 * t));
+        }
+      }
     }
   }
 }
@@ -206,16 +261,24 @@ thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, cons
   const NextTokens next{next_tok, has_next};
   size_t bytes = static_cast<size_t>(2) * (n + 1) * sizeof(int32_t);
   bool in_smem = bytes <= static_cast<size_t>(kSmemBudget);
-  int64_t grid = (static_cast<int64_t>(T) + kLabelThreads - 1) / kLabelThreads;
+  const int64_t per_block = static_cast<int64_t>(kLabelThreads) * kPerLane;  // positions
+  int64_t grid = (static_cast<int64_t>(T) + per_block - 1) / per_block;
   int64_t cap = static_cast<int64_t>(sm_count()) * 2;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   const dim3 blocks(static_cast<unsigned>(grid));
+  const bool vec = T % kPerLane == 0 && reinterpret_cast<uintptr_t>(labels) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(lmask) % 4 == 0 && reinterpret_cast<uintptr_t>(valid) % 4 == 0;
+  const size_t smem = in_smem ? bytes : 0;
   const cudaError_t e =
-      in_smem ? launch_pdl(roll_labels_kernel<true>, blocks, kLabelThreads, bytes, s, tokens, cu_v, cu, n, T, depth,
-                           fill, next, labels, lmask, valid, status)
-              : launch_pdl(roll_labels_kernel<false>, blocks, kLabelThreads, 0, s, tokens, cu_v, cu, n, T, depth, fill,
-                           next, labels, lmask, valid, status);
+      vec ? (in_smem ? launch_pdl(roll_labels_kernel<true, true>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu, n,
+                                  T, depth, fill, next, labels, lmask, valid, status)
+                     : launch_pdl(roll_labels_kernel<false, true>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu, n,
+                                  T, depth, fill, next, labels, lmask, valid, status))
+          : (in_smem ? launch_pdl(roll_labels_kernel<true, false>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu,
+                                  n, T, depth, fill, next, labels, lmask, valid, status)
+                     : launch_pdl(roll_labels_kernel<false, false>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu,
+                                  n, T, depth, fill, next, labels, lmask, valid, status));
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
