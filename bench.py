@@ -64,6 +64,8 @@ def parse_args():
     p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-other-configs", action="store_true",
+                   help="skip the swap / route timings of the other full-size workloads")
     return p.parse_args()
 
 
@@ -241,6 +243,44 @@ def make_inputs(w, device, rank):
         return None, None, raw
     cu = W.boundaries(W.doc_lengths(w.name))
     return cu, cu[-1], None
+
+
+# ---------------------------------------------------------------------------
+# timing helpers (CUDA events on the launching stream)
+# ---------------------------------------------------------------------------
+
+def single_us(fn, stream, device, reps=30, skip=10):
+    """Median duration of one launch between two CUDA events, the GPU kept
+    busy ahead of it so host launch latency is not counted."""
+    ts = []
+    for it in range(reps):
+        torch.cuda._sleep(200_000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        if it >= skip:
+            ts.append(a.elapsed_time(b) * 1e3)
+    return round(statistics.median(ts), 2)
+
+
+def back_to_back_us(fn, stream, device, launches=20, reps=12, skip=2):
+    """Per-launch duration of `launches` launches back to back between two
+    CUDA events (each launch waits for the one before, so launch latency
+    overlaps the previous launch), median over reps."""
+    ts = []
+    for it in range(reps):
+        torch.cuda._sleep(200_000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(launches):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        if it >= skip:
+            ts.append(a.elapsed_time(b) * 1e3 / launches)
+    return round(statistics.median(ts), 2)
 
 
 # ---------------------------------------------------------------------------
@@ -555,11 +595,44 @@ def run_thd(args, rank, world, local):
                    "frac_of_measured": round(swap_bytes / t3 / 1e3 / peak_gbs, 4),
                    "vs_fused": "same algorithmic bytes (2 x T x row_bytes) as one fused swap"}
 
+    # The swap in steady state: a model step does other work between swaps,
+    # so a swap's input is not the previous launch's output.  Three
+    # input/output buffer pairs in rotation (directions alternating): no swap
+    # reads what the launch before it wrote, and the dirty lines the previous
+    # launch left in L2 are written back during this one.
+    steady = None
+    if layers > 0:
+        ins = [x] + [x.clone() for _ in range(2)]
+        outs = [torch.empty_like(x) for _ in range(3)]
+        routes = (fwd, bwd)
+        k_box = [0]
+
+        def rotating_swap():
+            k = k_box[0]
+            k_box[0] += 1
+            lib.thd_swap(ins[k % 3].data_ptr(), outs[k % 3].data_ptr(), row_bytes, ctypes.byref(routes[k % 2].c),
+                         status.data_ptr(), sp)
+
+        steady_us = back_to_back_us(rotating_swap, stream, device, launches=30, reps=8, skip=2)
+        if thd.status_read(status) != 0:
+            raise RuntimeError("device status set by the rotating-buffer swaps")
+        peak_gbs, _ = measured_peak()
+        steady = {"us_per_launch": steady_us, "gbs": round(swap_bytes / steady_us / 1e3, 1),
+                  "frac_of_measured": round(swap_bytes / steady_us / 1e3 / peak_gbs, 4),
+                  "method": "3 input/output buffer pairs in rotation, directions alternating (no swap reads the "
+                            "previous launch's output); 30 launches back to back between CUDA events, per launch, "
+                            "median of 6"}
+        del ins, outs
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes,
                       steps=max(12, args.steps))
+
+    others = None
+    if not args.no_other_configs:
+        others = run_other_configs(thd, lib, w.name, device, stream, status)
 
     peak, peak_kind = measured_peak()
     traffic = swap_traffic_record(w.name)
@@ -604,6 +677,8 @@ def run_thd(args, rank, world, local):
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
             "algorithmic_bytes_per_launch": swap_bytes,
+            "frac_dram_bytes": (round(traffic / (swap_us * 1e-6) / 1e9 / peak, 4) if traffic else None),
+            "frac_steady_state": steady["frac_of_measured"] if steady else None,
         },
         "gpu_launches": launches_per_step * n_ev * world,   # every rank's, like value
         "clocks": clock_rec,
@@ -616,7 +691,81 @@ def run_thd(args, rank, world, local):
         result["data_prep_kernels"] = prep
     if uly is not None:
         result["ulysses_swap"] = uly
+    if steady is not None:
+        result["swap_steady_state"] = steady
+    if others:
+        result["other_configs"] = others
     return result, dict(x=x, T=T, cu=cu_d, w=w, row_bytes=row_bytes)
+
+
+def run_other_configs(thd, lib, current, device, stream, status):
+    """The second 128K workload (longtail128k: cp=8, 8 KiB rows) and the
+    route-build stress workload (stress16: cp=16, 4,096 documents, 512 B
+    rows), timed with the same CUDA-event method as the benchmarked
+    workload: route pair and partition (single launch and back to back) and
+    the swap pair (20 launches back to back, directions alternating, per
+    launch).  After timing, the payload must have come back unchanged (each
+    z->c swap is undone by the next c->z swap)."""
+    import ctypes
+
+    peak_gbs, peak_kind = measured_peak()
+    sp = stream.cuda_stream
+    out = {}
+    for name in ("longtail128k", "stress16"):
+        if name == current:
+            continue
+        w = W.BY_NAME[name]
+        cu_list = W.boundaries(W.doc_lengths(name))
+        T, cp, n_docs = cu_list[-1], w.cp, len(cu_list) - 1
+        cu_d = torch.tensor(cu_list, dtype=torch.int32, device=device)
+        x = W.payload_device(w.seed, T, w.hidden, device)
+        x0 = x.clone()
+        y = torch.empty_like(x)
+        fwd = thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device)
+        bwd = thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device)
+        pidx = torch.empty((cp, T // cp), dtype=torch.int32, device=device)
+        rb = w.row_bytes
+
+        def pair():
+            lib.thd_route_build_pair(cu_d.data_ptr(), n_docs, T, cp, ctypes.byref(fwd.c), ctypes.byref(bwd.c),
+                                     status.data_ptr(), sp)
+
+        def part():
+            lib.thd_partition_indices(cu_d.data_ptr(), n_docs, T, cp, -1, pidx.data_ptr(), status.data_ptr(), sp)
+
+        k_box = [0]
+
+        def swap():
+            k = k_box[0]
+            k_box[0] += 1
+            a, b, r = (x, y, fwd) if k % 2 == 0 else (y, x, bwd)
+            lib.thd_swap(a.data_ptr(), b.data_ptr(), rb, ctypes.byref(r.c), status.data_ptr(), sp)
+
+        pair()
+        torch.cuda.synchronize(device)
+        route = {"both_directions": single_us(pair, stream, device),
+                 "both_directions_back_to_back": back_to_back_us(pair, stream, device),
+                 "partition": single_us(part, stream, device),
+                 "partition_back_to_back": back_to_back_us(part, stream, device)}
+        swap_us = back_to_back_us(swap, stream, device, launches=20, reps=10, skip=2)   # an even count per rep
+        torch.cuda.synchronize(device)
+        if thd.status_read(status) != 0 or not torch.equal(x, x0):
+            raise RuntimeError(f"{name}: device status set or the payload did not come back")
+        swap_bytes = 2 * T * rb
+        gbs = swap_bytes / swap_us / 1e3
+        out[name] = {"description": w.description, "cp_size": cp, "T": T, "num_docs": n_docs, "row_bytes": rb,
+                     "route_build_us": route,
+                     "swap": {"kernel": plan_kernel_name(rb), "us_per_launch": swap_us, "gbs": round(gbs, 1),
+                              "frac_of_measured": round(gbs / peak_gbs, 4),
+                              "frac_of_spec_8tbs": round(gbs / SPEC_HBM_GBS, 4),
+                              "rows_per_s": round(T / (swap_us * 1e-6), 1),
+                              "algorithmic_bytes_per_launch": swap_bytes},
+                     "method": "route: median single launch (GPU kept busy ahead) and 20 back to back per launch; "
+                               "swap: 20 launches back to back (z->c, c->z alternating), per launch, median of 8; "
+                               f"peak = {peak_kind} copy bandwidth {peak_gbs} GB/s"}
+        del x, x0, y, fwd, bwd, pidx
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes, steps=12, slots=3):

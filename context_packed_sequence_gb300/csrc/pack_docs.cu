@@ -24,7 +24,9 @@
 //      3. emit: every chunk writes its tokens, padding and boundaries.
 //    Scratch: two int64 per row, seven per chunk and two totals.
 //  * per row (thd_pack_docs_noalloc, whose scratch is a fixed array of four
-//    int64 per row): the same two phases with one block per raw row.
+//    int64 per row): the same phases with one block per raw row; above 512
+//    rows one block turns the rows' statistics into prefixes in place
+//    between them.
 #include "thd_internal.cuh"
 
 namespace thd {
@@ -102,43 +104,107 @@ pack_stats_kernel(const int32_t* raw, int64_t S, int32_t eod, int32_t trim, int3
   }
 }
 
+// Up to this many rows every emit block sums the statistics of the rows
+// before it itself (two launches); beyond it one block scans them first
+// (three launches), since the self-sums cost every block a pass over all rows.
+#ifndef THD_PACK_SELF_SCAN_ROWS
+#define THD_PACK_SELF_SCAN_ROWS 512
+#endif
+constexpr int32_t kSelfScanRows = THD_PACK_SELF_SCAN_ROWS;
+
+// One block over all rows (more than kSelfScanRows): each row's exclusive
+// prefixes replace its statistics in place, ws[r] = {valid end, documents
+// before, padded tokens before, valid tokens before}; the totals go to
+// `counts` (and THD_ERR_CAPACITY to the status word when they do not fit).
 __global__ void __launch_bounds__(kPackThreads)
-pack_emit_kernel(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t align, int32_t pad_id,
-                 int32_t* tokens, int64_t tok_cap, int32_t* cu_v, int32_t* cu, int64_t docs_cap,
-                 int64_t* counts, const int64_t* ws, int32_t* status) {
+pack_rows_scan_kernel(int32_t B, int64_t tok_cap, int64_t docs_cap, int32_t* cu_v, int32_t* cu, int64_t* counts,
+                      int64_t* ws, int32_t* status) {
   __shared__ int64_t tmp[32];
   pdl_wait_then_release();
   if (block_status_set(status)) return;
-  const int64_t b = blockIdx.x;
-  // where this row starts: sums over the rows before it, and the grand totals
-  int64_t d_before = 0, t_before = 0, v_before = 0, d_all = 0, t_all = 0;
-  for (int64_t r = threadIdx.x; r < B; r += blockDim.x) {
-    int64_t ve = ws[r * 4 + 0], nd = ws[r * 4 + 1], np = ws[r * 4 + 2];
-    if (r < b) {
-      d_before += nd;
-      t_before += np;
-      v_before += ve;
+  int64_t d_carry = 0, t_carry = 0, v_carry = 0;
+  for (int64_t base = 0; base < B; base += blockDim.x) {
+    const int64_t r = base + threadIdx.x;
+    int64_t ve = 0, nd = 0, np = 0;
+    if (r < B) {
+      ve = ws[r * 4 + 0];
+      nd = ws[r * 4 + 1];
+      np = ws[r * 4 + 2];
     }
-    d_all += nd;
-    t_all += np;
+    int64_t pass_d, pass_t, pass_v;
+    const int64_t d_before = block_exclusive_scan(nd, OpSum(), static_cast<int64_t>(0), tmp, &pass_d);
+    const int64_t t_before = block_exclusive_scan(np, OpSum(), static_cast<int64_t>(0), tmp, &pass_t);
+    const int64_t v_before = block_exclusive_scan(ve, OpSum(), static_cast<int64_t>(0), tmp, &pass_v);
+    if (r < B) {
+      ws[r * 4 + 1] = d_carry + d_before;
+      ws[r * 4 + 2] = t_carry + t_before;
+      ws[r * 4 + 3] = v_carry + v_before;
+    }
+    d_carry += pass_d;
+    t_carry += pass_t;
+    v_carry += pass_v;
   }
-  d_before = block_sum(d_before, tmp);
-  t_before = block_sum(t_before, tmp);
-  v_before = block_sum(v_before, tmp);
-  d_all = block_sum(d_all, tmp);
-  t_all = block_sum(t_all, tmp);
-  const bool over = d_all + 1 > docs_cap || t_all > tok_cap || t_all > INT32_MAX;
-  if (b == 0 && threadIdx.x == 0) {
-    counts[0] = d_all;
-    counts[1] = t_all;
-    if (over) {
+  if (threadIdx.x == 0) {
+    counts[0] = d_carry;
+    counts[1] = t_carry;
+    if (d_carry + 1 > docs_cap || t_carry > tok_cap || t_carry > INT32_MAX) {
       status_set(status, THD_ERR_CAPACITY);
     } else {
       cu[0] = 0;
       cu_v[0] = 0;
     }
   }
-  if (over) return;
+}
+
+// prefixed: pack_rows_scan_kernel has run (ws holds each row's prefixes and
+// counts the totals); else the block sums the rows before its own.
+__global__ void __launch_bounds__(kPackThreads)
+pack_emit_kernel(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t align, int32_t pad_id,
+                 int32_t* tokens, int64_t tok_cap, int32_t* cu_v, int32_t* cu, int64_t docs_cap,
+                 int64_t* counts, const int64_t* ws, bool prefixed, int32_t* status) {
+  __shared__ int64_t tmp[32];
+  pdl_wait_then_release();
+  // (with the separate scan, that kernel has set the status word when the
+  // capacities are too small)
+  if (block_status_set(status)) return;
+  const int64_t b = blockIdx.x;
+  // where this row starts: sums over the rows before it, and the grand totals
+  int64_t d_before = 0, t_before = 0, v_before = 0, d_all = 0, t_all = 0;
+  if (prefixed) {
+    d_before = ws[b * 4 + 1];
+    t_before = ws[b * 4 + 2];
+    v_before = ws[b * 4 + 3];
+    d_all = counts[0];
+    t_all = counts[1];
+  } else {
+    for (int64_t r = threadIdx.x; r < B; r += blockDim.x) {
+      int64_t ve = ws[r * 4 + 0], nd = ws[r * 4 + 1], np = ws[r * 4 + 2];
+      if (r < b) {
+        d_before += nd;
+        t_before += np;
+        v_before += ve;
+      }
+      d_all += nd;
+      t_all += np;
+    }
+    d_before = block_sum(d_before, tmp);
+    t_before = block_sum(t_before, tmp);
+    v_before = block_sum(v_before, tmp);
+    d_all = block_sum(d_all, tmp);
+    t_all = block_sum(t_all, tmp);
+    const bool over = d_all + 1 > docs_cap || t_all > tok_cap || t_all > INT32_MAX;
+    if (b == 0 && threadIdx.x == 0) {
+      counts[0] = d_all;
+      counts[1] = t_all;
+      if (over) {
+        status_set(status, THD_ERR_CAPACITY);
+      } else {
+        cu[0] = 0;
+        cu_v[0] = 0;
+      }
+    }
+    if (over) return;
+  }
 
   const int32_t* row = raw + b * S;
   const int64_t ve = ws[b * 4 + 0];
@@ -493,8 +559,14 @@ thd_status_t launch_pack_docs_rows(const int32_t* raw, int32_t B, int64_t S, int
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
+  const bool prefixed = B > kSelfScanRows;
+  if (prefixed && (e = launch_pdl(pack_rows_scan_kernel, 1, kPackThreads, 0, s, B, tok_cap, docs_cap, cu_v, cu,
+                                  counts, ws, status)) != cudaSuccess) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
   if ((e = launch_pdl(pack_emit_kernel, B, kPackThreads, 0, s, raw, B, S, eod, align, pad_id, tokens, tok_cap, cu_v,
-                      cu, docs_cap, counts, ws, status)) != cudaSuccess) {
+                      cu, docs_cap, counts, static_cast<const int64_t*>(ws), prefixed, status)) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }

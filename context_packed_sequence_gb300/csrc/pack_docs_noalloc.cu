@@ -15,40 +15,31 @@
 // variable of this translation unit.  Every GPU that loads the library holds
 // its own copy until the process exits.  Host code cannot use the array's
 // name as a device address (in host code it names a host-side stand-in), so
-// the device address is looked up once per device with cudaGetSymbolAddress,
-// with that device current, on the first call made on that device.
-#include <mutex>
-
+// every call looks the device address up with cudaGetSymbolAddress, with the
+// caller's device current.  The address belongs to the CUDA context, not to
+// the device number: a context created after cudaDeviceReset, or another
+// context on the same device, has its own copy of the array at its own
+// address, so nothing is cached between calls.  The lookup allocates
+// nothing.  The first call in a context may load the library's device code
+// into it (lazy module loading), so make that call before any stream capture.
 #include "thd_internal.cuh"
 
 namespace thd {
 namespace {
 
 constexpr int32_t kNoAllocMaxRows = THD_PACK_NOALLOC_MAX_ROWS;
-constexpr int kMaxDevices = 64;
 
-// Scratch shared by every call on a device.  No entry needs to start at
-// zero: each call's first kernel writes all four entries of every row its
-// second kernel reads, so nothing is carried over from the previous call.
+// Scratch shared by every call in a context.  No entry needs to start at
+// zero: each call's first kernel writes all four entries of every row the
+// later kernels read, so nothing is carried over from the previous call.
 static __device__ __align__(256) int64_t g_pack_scratch[kNoAllocMaxRows * 4];
 
-std::mutex g_scratch_mutex;
-int64_t* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_pack_scratch on the current device (looked up once).
-cudaError_t scratch_for_current_device(int64_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+// Device address of g_pack_scratch in the current context.
+cudaError_t scratch_for_current_context(int64_t** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_pack_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_pack_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<int64_t*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  *out = static_cast<int64_t*>(p);
   return cudaSuccess;
 }
 
@@ -69,7 +60,7 @@ extern "C" thd_status_t thd_pack_docs_noalloc(const int32_t* raw, int32_t B, int
     return THD_ERR_INVALID_ARG;
   if (B > 0 && S > 0 && (!raw || !tokens_out)) return THD_ERR_INVALID_ARG;
   int64_t* scratch = nullptr;
-  cudaError_t e = scratch_for_current_device(&scratch);
+  cudaError_t e = scratch_for_current_context(&scratch);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

@@ -332,9 +332,13 @@ thd_status_t thd_pack_docs(const int32_t *raw, int32_t B, int64_t S, int32_t eod
  * that loads the library until the process exits:
  *  - B > THD_PACK_NOALLOC_MAX_ROWS returns THD_ERR_SCRATCH_LIMIT at once and
  *    enqueues nothing (use thd_pack_docs with your own workspace then);
- *  - the first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any
- *    stream capture;
+ *  - every call looks up the array's device address in the current context
+ *    (the address belongs to the context: after cudaDeviceReset, or in
+ *    another context on the same device, it differs), which allocates
+ *    nothing; the first call in a context may load the library's device
+ *    code into it, so make that call before any stream capture;
+ *  - above 512 rows a third kernel turns the rows' statistics into prefix
+ *    sums in the array between the two packing kernels;
  *  - all calls on a device share the one array, so calls that may overlap on
  *    the GPU (different streams, no ordering between them) race and must be
  *    serialised by the caller.  Calls in order on one stream are safe: each

@@ -29,7 +29,7 @@ Sources (web pages, cited by title and section):
   chunk 2*cp-1-r), section 3 (the worked example B=2, S=8, CP=2) and
   section 3.8 (the EOD position's label is masked).
 
-Readings taken where the pages are silent (each one is listed in the design doc):
+Readings taken where the pages are silent:
 
 * contiguous layout: rank r holds the global rows [r*T/cp, (r+1)*T/cp)
   ([PR273] 2.1 "one interval per rank"; [PSCP] 2.5 slices Ulysses the same way);

@@ -1,8 +1,8 @@
 """GPU vs oracle, element by element (integers and raw bytes: tolerance 0).
 
-Small and medium cases are compared in full; the full-size workloads compare
-the whole route exactly and the payload on sampled rows, plus the round trip
-z->c->z on every byte."""
+Every case is compared in full: small and medium ones against the oracle's
+outputs, the full-size workloads' routes entry by entry and their payloads
+row by row against the oracle's permutation (plus the round trip z->c->z)."""
 
 import numpy as np
 import pytest
@@ -625,25 +625,29 @@ def test_pack_docs_many_chunks_and_rows():
 # the full-size workloads, in the launch configuration the benchmark times
 # --------------------------------------------------------------------------
 
-def _full_size_swap_check(cu, cp, hidden, seed, sample=4096):
+def _full_size_swap_check(cu, cp, hidden, seed):
+    """Both routes exactly, then every row of both directions' payloads
+    against the oracle's permutation (target row q = source row
+    src_of_dst[q], the oracle's pack -> all-to-all -> scatter composed; the
+    oracle tests pin the two to each other), and the round trip."""
     T = cu[-1]
     x = W.payload_device(seed, T, hidden, "cuda")
     pair = _gpu_pair(cu, T, cp)
+    outs = {}
     for d in (Z2C, C2Z):
         o = oracle.build_route(cu, T, cp, d)
         r = _gpu_route(cu, T, cp, d)
         _assert_route(r, o)
         _assert_route(pair[d], o)
         st = thd.new_status()
-        out = thd.swap(x, r, status=st)
+        src = x if d == Z2C else outs[Z2C]
+        out = thd.swap(src, r, status=st)
         thd.check_status(st)
-        rows = np.random.default_rng(seed + d).integers(0, T, size=sample)
-        src = torch.tensor([o.src_of_dst[q] for q in rows], device="cuda").long()
-        assert torch.equal(out[torch.from_numpy(rows).cuda().long()], x[src])
-        if d == Z2C:
-            fwd = out
-    back = thd.swap(fwd, _gpu_route(cu, T, cp, C2Z))
-    assert torch.equal(back, x)
+        perm = torch.tensor(o.src_of_dst, dtype=torch.int64, device="cuda")
+        assert torch.equal(out, src[perm]), f"direction {d}: a row differs from the oracle's"
+        del perm
+        outs[d] = out
+    assert torch.equal(outs[C2Z], x)
 
 
 @pytest.mark.parametrize("name", ["lognorm128k", "longtail128k", "stress16"])
@@ -654,11 +658,13 @@ def test_full_size_workloads(name):
 
 
 @pytest.mark.parametrize("name", ["lognorm128k", "longtail128k", "stress16"])
-def test_full_size_ulysses(name, sample=4096):
-    """The Ulysses exchange of the full hidden states: sampled tokens against
-    the oracle, every byte by the round trip.  stress16 splits 512-byte rows
-    16 ways (32-byte pieces, the tile transpose); the 128K workloads have
-    1 KiB pieces (the bulk row engine)."""
+def test_full_size_ulysses(name, chunk=65536):
+    """The Ulysses exchange of the full hidden states, every token against the
+    oracle (in chunks of tokens, each a sequence of its own for the oracle:
+    the exchange moves every token's pieces independently), head -> sequence
+    by the round trip.  stress16 splits 512-byte rows 16 ways (32-byte
+    pieces, the tile transpose); the 128K workloads have 1 KiB pieces (the
+    bulk row engine)."""
     w = W.BY_NAME[name]
     T = sum(W.doc_lengths(name))
     x = W.payload_device(w.seed, T, w.hidden, "cuda")
@@ -667,13 +673,14 @@ def test_full_size_ulysses(name, sample=4096):
     y = thd.ulysses_swap(x, w.cp, thd.SEQ_TO_HEAD, status=st)
     back = thd.ulysses_swap(y, w.cp, thd.HEAD_TO_SEQ, status=st)
     thd.check_status(st)
-    rows = np.sort(np.random.default_rng(w.seed).choice(T, size=sample - sample % w.cp, replace=False))
-    idx = torch.from_numpy(rows).cuda().long()
-    xs = x[idx].contiguous().view(torch.uint8).reshape(len(rows), -1).cpu().numpy()
-    want = oracle.ulysses_swap(xs, w.cp, oracle.SEQ_TO_HEAD).reshape(w.cp, len(rows), -1)
-    got = y[:, idx].contiguous().view(torch.uint8).reshape(w.cp, len(rows), -1).cpu().numpy()
     assert y.shape[2] == heads // w.cp
-    assert np.array_equal(got, want)
+    assert chunk % w.cp == 0 and T % w.cp == 0
+    for lo in range(0, T, chunk):
+        hi = min(T, lo + chunk)
+        xs = x[lo:hi].contiguous().view(torch.uint8).reshape(hi - lo, -1).cpu().numpy()
+        want = oracle.ulysses_swap(xs, w.cp, oracle.SEQ_TO_HEAD).reshape(w.cp, hi - lo, -1)
+        got = y[:, lo:hi].contiguous().view(torch.uint8).reshape(w.cp, hi - lo, -1).cpu().numpy()
+        assert np.array_equal(got, want), f"tokens [{lo}, {hi})"
     assert torch.equal(back, x)
 
 
@@ -694,7 +701,7 @@ def test_full_size_pipeline():
     zl, zm, zv = thd.roll_labels_zigzag(tok, cu_v, cu, w.cp, w.mtp_depth, fill=0)
     idx = torch.tensor(oracle.partition_indices(cu_o, len(tok_o), w.cp, -1), device="cuda").long()
     assert torch.equal(zl, labels[:, idx]) and torch.equal(zm, lmask[:, idx]) and torch.equal(zv, valid[idx])
-    _full_size_swap_check(cu_o, w.cp, w.hidden, w.seed, sample=2048)
+    _full_size_swap_check(cu_o, w.cp, w.hidden, w.seed)
 
 
 def test_pipeline_fuzz():
