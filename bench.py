@@ -64,6 +64,9 @@ def parse_args():
     p.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cp-exchange", action="store_true",
+                   help="one CP rank per GPU (--gpus = the workload's cp): the conversion between GPUs, "
+                        "per-rank pack -> NCCL all-to-all -> per-rank scatter, instead of independent replicas")
     p.add_argument("--no-other-configs", action="store_true",
                    help="skip the swap / route timings of the other full-size workloads")
     return p.parse_args()
@@ -865,6 +868,74 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
             "link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
 
 
+def run_cp_exchange(args, rank, world, local):
+    """The conversion between GPUs: every rank is one CP rank holding its own
+    shard.  A step builds both routes on every GPU (no host synchronisation),
+    reads this rank's split sizes and identity flags to the host once per
+    direction (the collective needs them there), then runs every layer's
+    z->c and c->z exchange (per-rank pack kernel, NCCL all_to_all_single,
+    per-rank scatter kernel).  value = payload bytes of the whole batch per
+    conversion (2 x T x row_bytes, read + write), summed over conversions,
+    per second of the slowest rank's step time."""
+    import context_packed_sequence_gb300 as thd
+
+    w = W.BY_NAME[args.workload]
+    if w.name == "pipeline" or w.cp != world:
+        raise SystemExit(f"--cp-exchange needs --gpus equal to the workload's cp ({w.name}: cp={w.cp}, "
+                         f"world={world}) and a workload with fixed boundaries")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    layers = args.layers if args.layers is not None else 48
+    cu_list = W.boundaries(W.doc_lengths(w.name))
+    T, cp = cu_list[-1], w.cp
+    S = T // cp
+    cu_d = torch.tensor(cu_list, dtype=torch.int32, device=device)
+    shard = W.payload_device(w.seed, T, w.hidden, device)[rank * S:(rank + 1) * S].clone()   # zigzag shard
+    status = thd.new_status(device)
+    routes = (thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device), thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device))
+
+    launches = [0]
+
+    def step():
+        fwd, bwd = thd.route_build_pair(cu_d, T, cp, status=status, routes=routes)
+        ex_f, ex_b = thd.CpExchange.from_route(fwd, rank), thd.CpExchange.from_route(bwd, rank)
+        # libthd kernels per step: the route build, then pack and scatter of
+        # every exchange unless that side is the identity (zero-copy)
+        launches[0] = 1 + layers * sum(2 - e.send_identity - e.recv_identity for e in (ex_f, ex_b))
+        a = shard
+        for _ in range(layers):
+            a = ex_b(ex_f(a))
+        return a
+
+    for _ in range(args.warmup):
+        back = step()
+    torch.cuda.synchronize(device)
+    if not torch.equal(back, shard):
+        raise RuntimeError("the exchanges there and back did not return the shard")
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    conv_bytes = 2 * T * w.row_bytes
+    value = conv_bytes * 2 * layers * args.steps / (ms / 1e3) / 1e9
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "int32", "data": "synthetic", "mode": "cp_exchange",
+        "config": {"workload": w.name, "cp_size": cp, "T": T, "row_bytes": w.row_bytes, "layers": layers,
+                   "parallelism": f"cp{cp}: one CP rank per GPU, per-rank pack/scatter kernels around an NCCL "
+                                  "all_to_all_single; split sizes read to the host once per direction per step"},
+        "gpu_launches": int(sum_over_ranks(float(launches[0] * args.steps), world, device)),
+    }
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (cpu_baseline leg and --impl reference)
 # ---------------------------------------------------------------------------
@@ -962,6 +1033,11 @@ def main():
             return
         if not torch.cuda.is_available():
             raise SystemExit("bench.py: the thd arm needs a CUDA GPU")
+        if args.cp_exchange:
+            res = run_cp_exchange(args, rank, world, local)
+            if rank == 0:
+                print(json.dumps(res), flush=True)
+            return
         res, _ = run_thd(args, rank, world, local)
         if rank == 0:
             if not args.no_cpu_baseline and world == 1:

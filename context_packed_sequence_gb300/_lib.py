@@ -87,6 +87,10 @@ SIGNATURES = {
     "thd_partition_indices": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_int32, c_void_p,
                                         c_void_p, c_void_p]),
     "thd_swap": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
+    "thd_swap_batched": (c_int32, [c_void_p, c_void_p, c_int64, c_int64, POINTER(ThdRoute), c_void_p,
+                                   c_void_p]),
+    "thd_pack_rank": (c_int32, [c_void_p, c_void_p, c_int32, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
+    "thd_scatter_rank": (c_int32, [c_void_p, c_void_p, c_int32, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
     "thd_pack": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
     "thd_a2a_local": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),
     "thd_scatter": (c_int32, [c_void_p, c_void_p, c_int64, POINTER(ThdRoute), c_void_p, c_void_p]),

@@ -252,6 +252,76 @@ def scatter(recv, route: Route, out=None, status=None, stream=None):
     return _copy("thd_scatter", recv, route, out, status, stream)
 
 
+def swap_seq_dim(x, route: Route, seq_dim: int, out=None, status=None, stream=None):
+    """The fused swap along dimension ``seq_dim`` of a contiguous tensor:
+    out.select(seq_dim, q) = x.select(seq_dim, route.src_of_dst[q]).
+
+    The dims before seq_dim are independent blocks that share the route and
+    the dims after it are the row payload, so [outer, T, inner...] moves with
+    one thd_swap_batched launch and no transposed copy."""
+    _need_cuda(x, "x")
+    seq_dim = seq_dim % x.dim()
+    if x.shape[seq_dim] != route.T:
+        raise ValueError(f"x must have {route.T} rows along dim {seq_dim}, got shape {tuple(x.shape)}")
+    if x.device != route.device:
+        raise ValueError(f"x is on {x.device}, the route on {route.device}")
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda(out, "out")
+    if out.shape != x.shape or out.dtype != x.dtype or out.device != x.device:
+        raise ValueError("out must match x in shape, dtype and device")
+    if x.numel() == 0:
+        return out
+    if status is None:
+        status = getattr(route, "status", None)
+    outer = 1
+    for n in x.shape[:seq_dim]:
+        outer *= int(n)
+    row_bytes = x.numel() // (outer * route.T) * x.element_size()
+    with _range("thd_swap_batched"):
+        code = L.load().thd_swap_batched(_ptr(x), _ptr(out), outer, row_bytes, ctypes.byref(route.c), _ptr(status),
+                                         _stream(stream))
+    _raise_host(code, "thd_swap_batched")
+    return out
+
+
+def _rank_copy(fn_name, x, route, rank, out, status, stream):
+    _need_cuda(x, "x")
+    if not 0 <= int(rank) < route.cp:
+        raise ValueError(f"cp_rank must be in [0, {route.cp}), got {rank}")
+    if x.dim() < 1 or x.shape[0] != route.S:
+        raise ValueError(f"a shard must have {route.S} rows, got shape {tuple(x.shape)}")
+    if x.device != route.device:
+        raise ValueError(f"x is on {x.device}, the route on {route.device}")
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda(out, "out")
+    if out.shape != x.shape or out.dtype != x.dtype or out.device != x.device:
+        raise ValueError("out must match x in shape, dtype and device")
+    if status is None:
+        status = getattr(route, "status", None)
+    if x.numel() == 0:
+        return out
+    row_bytes = x[0].numel() * x.element_size()
+    with _range(fn_name):
+        code = getattr(L.load(), fn_name)(_ptr(x), _ptr(out), int(rank), row_bytes, ctypes.byref(route.c),
+                                          _ptr(status), _stream(stream))
+    _raise_host(code, fn_name)
+    return out
+
+
+def pack_rank(shard, route: Route, rank: int, out=None, status=None, stream=None):
+    """One rank's send buffer from its own shard [S, ...]:
+    send[j] = shard[send_rows[rank][j]], grouped by destination rank."""
+    return _rank_copy("thd_pack_rank", shard, route, rank, out, status, stream)
+
+
+def scatter_rank(recv, route: Route, rank: int, out=None, status=None, stream=None):
+    """One rank's shard from its receive buffer [S, ...]:
+    out[recv_rows[rank][j]] = recv[j]."""
+    return _rank_copy("thd_scatter_rank", recv, route, rank, out, status, stream)
+
+
 def ulysses_swap(x, cp: int, direction: int, out=None, status=None, stream=None):
     """Ulysses exchange between sequence shards and head shards.
 
@@ -448,12 +518,17 @@ def zigzag_contiguous_thd_swap(x, cu_seqlens_padded, cp: int, direction: int, se
 
     x holds all cp virtual ranks' shards of the packed sequence along seq_dim
     (rank-major).  cp == 1 returns x itself (nothing moves), as the pages'
-    swap does.  Other dims are carried along as the row payload."""
+    swap does.  The pages move the sequence dim to the front, make the tensor
+    contiguous, swap and move it back (Relax PR #273, section 2.6); here a
+    contiguous x of any seq_dim moves in one launch (the dims before seq_dim
+    are independent blocks, the dims after it the row payload), with no
+    transposed copy.  A non-contiguous x is compacted first."""
     if cp == 1:
         return x
+    seq_dim = seq_dim % x.dim()
     T = x.shape[seq_dim]
     route = cache.get(cu_seqlens_padded, T, cp, direction, status, stream) if cache is not None else \
         route_build(cu_seqlens_padded, T, cp, direction, status=status, stream=stream)
-    xs = x.movedim(seq_dim, 0).contiguous()
-    out = swap(xs, route, status=route.status if status is None else status, stream=stream)
-    return out.movedim(0, seq_dim)
+    if not x.is_contiguous():
+        x = x.contiguous()
+    return swap_seq_dim(x, route, seq_dim, status=route.status if status is None else status, stream=stream)

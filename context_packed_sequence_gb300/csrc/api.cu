@@ -40,6 +40,16 @@ thd_status_t copy_entry(CopyKind kind, const void* src, void* dst, int64_t row_b
   if (ranges_overlap(src, dst, bytes)) return THD_ERR_INVALID_ARG;
   return launch_copy(kind, src, dst, row_bytes, route, d_status, stream);
 }
+
+thd_status_t rank_copy_entry(bool scatter, const void* src, void* dst, int32_t cp_rank, int64_t row_bytes,
+                             const thd_route_t* route, int32_t* d_status, cudaStream_t stream) {
+  if (!route_ok(route) || row_bytes <= 0 || row_bytes > kMaxRowBytes) return THD_ERR_INVALID_ARG;
+  if (cp_rank < 0 || cp_rank >= route->cp_size) return THD_ERR_INVALID_ARG;
+  const int64_t bytes = route->total_rows / route->cp_size * row_bytes;
+  if (bytes > 0 && (!src || !dst)) return THD_ERR_INVALID_ARG;
+  if (ranges_overlap(src, dst, bytes)) return THD_ERR_INVALID_ARG;
+  return launch_rank_copy(scatter, src, dst, cp_rank, row_bytes, route, d_status, stream);
+}
 }  // namespace
 
 void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int32_t>(e); }
@@ -136,6 +146,26 @@ thd_status_t thd_partition_indices(const int32_t* cu_seqlens_padded, int32_t num
 thd_status_t thd_swap(const void* src, void* dst, int64_t row_bytes, const thd_route_t* route,
                       int32_t* d_status, cudaStream_t stream) {
   return copy_entry(COPY_SWAP, src, dst, row_bytes, route, d_status, stream);
+}
+
+thd_status_t thd_swap_batched(const void* src, void* dst, int64_t outer, int64_t row_bytes,
+                              const thd_route_t* route, int32_t* d_status, cudaStream_t stream) {
+  if (!route_ok(route) || row_bytes <= 0 || row_bytes > kMaxRowBytes || outer < 0) return THD_ERR_INVALID_ARG;
+  if (outer * route->total_rows > kMaxRows) return THD_ERR_INVALID_ARG;
+  const int64_t bytes = outer * route->total_rows * row_bytes;
+  if (bytes > 0 && (!src || !dst)) return THD_ERR_INVALID_ARG;
+  if (ranges_overlap(src, dst, bytes)) return THD_ERR_INVALID_ARG;
+  return launch_swap_batched(src, dst, static_cast<int32_t>(outer), row_bytes, route, d_status, stream);
+}
+
+thd_status_t thd_pack_rank(const void* src_shard, void* send_buf, int32_t cp_rank, int64_t row_bytes,
+                           const thd_route_t* route, int32_t* d_status, cudaStream_t stream) {
+  return rank_copy_entry(false, src_shard, send_buf, cp_rank, row_bytes, route, d_status, stream);
+}
+
+thd_status_t thd_scatter_rank(const void* recv_buf, void* dst_shard, int32_t cp_rank, int64_t row_bytes,
+                              const thd_route_t* route, int32_t* d_status, cudaStream_t stream) {
+  return rank_copy_entry(true, recv_buf, dst_shard, cp_rank, row_bytes, route, d_status, stream);
 }
 
 thd_status_t thd_pack(const void* src, void* send_buf, int64_t row_bytes, const thd_route_t* route,

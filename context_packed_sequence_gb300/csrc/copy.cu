@@ -72,6 +72,31 @@ struct RankLocalMap {
   }
 };
 
+// fused swap of `outer` independent [T][row] blocks through one route (a
+// tensor whose sequence dim is not the first, [outer][T][row] in memory):
+// target row o*T + q takes source row o*T + src_of_dst[q]
+struct BatchedSwapMap {
+  const int32_t* idx;
+  int32_t T;
+  FastDiv divT;
+  __device__ __forceinline__ int32_t operator()(int32_t q) const {
+    const int32_t o = divT.div(q), qq = q - o * T;
+    const int32_t v = __ldg(idx + qq);
+    return (v >= 0 && v < T) ? o * T + v : -1;
+  }
+};
+
+// one rank's shard: linear row j <-> local row rows[j] of the same rank (the
+// per-rank pack and scatter of a caller that holds only its own shard)
+struct OneRankMap {
+  const int32_t* idx;  // the rank's S entries
+  int32_t S;
+  __device__ __forceinline__ int32_t operator()(int32_t j) const {
+    const int32_t v = __ldg(idx + j);
+    return (v >= 0 && v < S) ? v : -1;
+  }
+};
+
 // all-to-all: receive row j of rank d comes from the send buffer of the rank
 // s whose receive block holds j, at that block's offset in s's send buffer.
 struct A2AMap {
@@ -708,6 +733,27 @@ thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, i
     return launch_ulysses_tiles(src, dst, T, cp, row_bytes, seq_to_head, status, s);
   const UlyssesMap map{T, cp, seq_to_head, make_fast_div(seq_to_head ? T : cp)};
   return dispatch_unit<UlyssesMap, false>(src, dst, T * cp, row_bytes / cp, map, status, s);
+}
+
+thd_status_t launch_swap_batched(const void* src, void* dst, int32_t outer, int64_t row_bytes,
+                                 const thd_route_t* r, int32_t* status, cudaStream_t s) {
+  const int32_t T = static_cast<int32_t>(r->total_rows);
+  if (T == 0 || outer == 0) return THD_OK;
+  // outer * T < 2^31 (checked by the caller): the engines index rows with int32
+  return dispatch_unit<BatchedSwapMap, false>(src, dst, outer * T, row_bytes,
+                                              BatchedSwapMap{r->src_of_dst, T, make_fast_div(T)}, status, s);
+}
+
+thd_status_t launch_rank_copy(bool scatter, const void* src, void* dst, int32_t rank, int64_t row_bytes,
+                              const thd_route_t* r, int32_t* status, cudaStream_t s) {
+  const int32_t T = static_cast<int32_t>(r->total_rows);
+  const int32_t S = T / r->cp_size;
+  if (S == 0) return THD_OK;
+  const int64_t off = static_cast<int64_t>(rank) * S;
+  if (scatter)  // dst_shard[recv_rows[rank][j]] = recv[j]
+    return dispatch_unit<OneRankMap, true>(src, dst, S, row_bytes, OneRankMap{r->recv_rows + off, S}, status, s);
+  // send[j] = src_shard[send_rows[rank][j]]
+  return dispatch_unit<OneRankMap, false>(src, dst, S, row_bytes, OneRankMap{r->send_rows + off, S}, status, s);
 }
 
 thd_status_t launch_copy(CopyKind kind, const void* src, void* dst, int64_t row_bytes,

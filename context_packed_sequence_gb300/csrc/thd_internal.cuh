@@ -407,6 +407,12 @@ thd_status_t launch_partition(const int32_t* cu, int32_t n, int32_t T, int32_t c
 enum CopyKind { COPY_SWAP = 0, COPY_PACK = 1, COPY_A2A = 2, COPY_SCATTER = 3 };
 thd_status_t launch_copy(CopyKind kind, const void* src, void* dst, int64_t row_bytes,
                          const thd_route_t* route, int32_t* status, cudaStream_t s);
+// outer independent [T][row] blocks through one route (outer * T < 2^31)
+thd_status_t launch_swap_batched(const void* src, void* dst, int32_t outer, int64_t row_bytes,
+                                 const thd_route_t* route, int32_t* status, cudaStream_t s);
+// one rank's pack (scatter = false) or scatter on [S][row] shards
+thd_status_t launch_rank_copy(bool scatter, const void* src, void* dst, int32_t rank, int64_t row_bytes,
+                              const thd_route_t* route, int32_t* status, cudaStream_t s);
 thd_status_t launch_ulysses(const void* src, void* dst, int32_t T, int32_t cp, int64_t row_bytes, bool seq_to_head,
                             int32_t* status, cudaStream_t s);
 // tile transpose for head-group pieces below 1 KiB (multiples of 16 bytes,

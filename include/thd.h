@@ -190,6 +190,20 @@ thd_status_t thd_partition_indices(const int32_t *cu_seqlens_padded, int32_t num
 thd_status_t thd_swap(const void *src, void *dst, int64_t row_bytes, const thd_route_t *route,
                       int32_t *d_status, cudaStream_t stream);
 
+/*
+ * thd_swap over `outer` independent blocks of T rows that share one route:
+ * src and dst are [outer][T][row_bytes] in memory, and for every o < outer
+ *   dst[o][q] = src[o][route->src_of_dst[q]].
+ * This is the layout conversion of a tensor whose sequence dimension is not
+ * the first one -- [outer, T, inner...] contiguous, row = the inner
+ * dimensions -- done in place of the movedim + contiguous + swap + movedim
+ * that the pages wrap around the conversion (Relax PR #273, section 2.6),
+ * with no transposed copy.  outer * T < 2^31; outer == 0 moves nothing.
+ * Buffers, row_bytes and d_status follow thd_swap's rules.
+ */
+thd_status_t thd_swap_batched(const void *src, void *dst, int64_t outer, int64_t row_bytes,
+                              const thd_route_t *route, int32_t *d_status, cudaStream_t stream);
+
 /* The three steps the pages run (Relax PR #273, section 2.1), for every
  * virtual rank at once; buffers are [cp][S][row_bytes], must not overlap, and
  * follow thd_swap's rules for row_bytes, alignment and d_status.
@@ -203,6 +217,31 @@ thd_status_t thd_a2a_local(const void *send_buf, void *recv_buf, int64_t row_byt
                            const thd_route_t *route, int32_t *d_status, cudaStream_t stream);
 thd_status_t thd_scatter(const void *recv_buf, void *dst, int64_t row_bytes,
                          const thd_route_t *route, int32_t *d_status, cudaStream_t stream);
+
+/*
+ * One rank's pack and scatter, for a caller that holds only its own shard
+ * (one context-parallel rank per GPU; Relax PR #273, sections 2.1-2.2: each
+ * rank packs its rows into a send buffer grouped by destination, exchanges
+ * them with an all-to-all of input/output split sizes, and scatters what it
+ * receives).  Every buffer is [S][row_bytes], S = T / cp_size, local to rank
+ * cp_rank (0 <= cp_rank < cp_size):
+ *  thd_pack_rank:    send_buf[j] = src_shard[send_rows[cp_rank][j]]
+ *  thd_scatter_rank: dst_shard[recv_rows[cp_rank][j]] = recv_buf[j]
+ * Between them, rank cp_rank sends send_buf rows [send_offsets[cp_rank][d],
+ * send_offsets[cp_rank][d+1]) to rank d and receives from rank s into
+ * recv_buf rows [recv_offsets[cp_rank][s], recv_offsets[cp_rank][s+1]): the
+ * all-to-all's split sizes are input_split_sizes[cp_rank][:] and
+ * output_split_sizes[cp_rank][:].  When send_identity[cp_rank]
+ * (recv_identity[cp_rank]) is set the pack (scatter) is a plain copy, which a
+ * caller that reads the flags may skip by handing over the shard itself
+ * ("identity = zero-copy", section 2.2).  The route is the one thd_route_build
+ * builds for all ranks from the same boundaries on every GPU.  Buffers,
+ * row_bytes and d_status follow thd_swap's rules.
+ */
+thd_status_t thd_pack_rank(const void *src_shard, void *send_buf, int32_t cp_rank, int64_t row_bytes,
+                           const thd_route_t *route, int32_t *d_status, cudaStream_t stream);
+thd_status_t thd_scatter_rank(const void *recv_buf, void *dst_shard, int32_t cp_rank, int64_t row_bytes,
+                              const thd_route_t *route, int32_t *d_status, cudaStream_t stream);
 
 /*
  * Ulysses sequence <-> head exchange ("Packed Sequence 与上下文并行",
