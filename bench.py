@@ -330,8 +330,7 @@ def run_thd(args, rank, world, local):
     row_bytes = w.row_bytes
     x = W.payload_device(w.seed + 1000 * rank, T, w.hidden, device)
     y = torch.empty_like(x)
-    fwd = thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device)
-    bwd = thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device)
+    fwd, bwd = thd.Route.pair(T, cp, device)   # one buffer, the common arrays shared
     pidx = torch.empty((cp, T // cp), dtype=torch.int32, device=device)
     swap_bytes = 2 * T * row_bytes
     launches_per_step = 2 + 2 * layers + (3 if extra is not None else 0)
@@ -724,8 +723,7 @@ def run_other_configs(thd, lib, current, device, stream, status):
         x = W.payload_device(w.seed, T, w.hidden, device)
         x0 = x.clone()
         y = torch.empty_like(x)
-        fwd = thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device)
-        bwd = thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device)
+        fwd, bwd = thd.Route.pair(T, cp, device)
         pidx = torch.empty((cp, T // cp), dtype=torch.int32, device=device)
         rb = w.row_bytes
 
@@ -794,7 +792,7 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
     yd = [torch.empty_like(x) for _ in range(slots)]
     cud = [torch.empty_like(cu_d) for _ in range(slots)]
     st = thd.new_status(device)
-    routes = (thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device), thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device))
+    routes = thd.Route.pair(T, cp, device)
     ks = torch.cuda.current_stream(device)
     ups, downs = torch.cuda.Stream(device), torch.cuda.Stream(device)
     cs = ups  # the link-only timings below
@@ -892,7 +890,7 @@ def run_cp_exchange(args, rank, world, local):
     cu_d = torch.tensor(cu_list, dtype=torch.int32, device=device)
     shard = W.payload_device(w.seed, T, w.hidden, device)[rank * S:(rank + 1) * S].clone()   # zigzag shard
     status = thd.new_status(device)
-    routes = (thd.Route(T, cp, thd.ZIGZAG_TO_CONTIGUOUS, device), thd.Route(T, cp, thd.CONTIGUOUS_TO_ZIGZAG, device))
+    routes = thd.Route.pair(T, cp, device)
 
     launches = [0]
 

@@ -80,6 +80,8 @@ class ThdRoute(ctypes.Structure):
 SIGNATURES = {
     "thd_route_bytes": (c_size_t, [c_int64, c_int32]),
     "thd_route_bind": (c_int32, [POINTER(ThdRoute), c_void_p, c_size_t, c_int64, c_int32, c_int32]),
+    "thd_route_pair_bytes": (c_size_t, [c_int64, c_int32]),
+    "thd_route_bind_pair": (c_int32, [POINTER(ThdRoute), POINTER(ThdRoute), c_void_p, c_size_t, c_int64, c_int32]),
     "thd_route_build": (c_int32, [c_void_p, c_int32, c_int64, c_int32, c_int32, POINTER(ThdRoute),
                                   c_void_p, c_void_p]),
     "thd_route_build_pair": (c_int32, [c_void_p, c_int32, c_int64, c_int32, POINTER(ThdRoute), POINTER(ThdRoute),

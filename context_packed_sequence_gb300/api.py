@@ -112,19 +112,22 @@ class Route:
     """One direction's all-to-all route for every virtual rank, in one device
     buffer (fields as in thd_route_t; tensors are views into the buffer)."""
 
-    def __init__(self, T: int, cp: int, direction: int, device=None):
+    def __init__(self, T: int, cp: int, direction: int, device=None, _bound=None):
         lib = L.load()
         if direction not in (ZIGZAG_TO_CONTIGUOUS, CONTIGUOUS_TO_ZIGZAG):
             raise ThdError(L.ERR_BAD_DIRECTION, "Route")
-        nbytes = lib.thd_route_bytes(int(T), int(cp))
-        if nbytes == 0:
-            raise ThdError(L.ERR_INVALID_ARG, f"Route(T={T}, cp={cp})")
         self.T, self.cp, self.direction = int(T), int(cp), int(direction)
+        if _bound is not None:  # (buffer, thd_route_t) bound by Route.pair
+            self._buf, self.c = _bound
+        else:
+            nbytes = lib.thd_route_bytes(self.T, self.cp)
+            if nbytes == 0:
+                raise ThdError(L.ERR_INVALID_ARG, f"Route(T={T}, cp={cp})")
+            self._buf = torch.empty(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
+            self.c = L.ThdRoute()
+            _raise_host(lib.thd_route_bind(ctypes.byref(self.c), self._buf.data_ptr(), nbytes, self.T, self.cp,
+                                           self.direction), "thd_route_bind")
         self.S = self.T // self.cp
-        self._buf = torch.empty(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
-        self.c = L.ThdRoute()
-        _raise_host(lib.thd_route_bind(ctypes.byref(self.c), self._buf.data_ptr(), nbytes, self.T, self.cp,
-                                       self.direction), "thd_route_bind")
         base = self._buf.data_ptr()
 
         def view(addr, n, dtype, shape):
@@ -146,6 +149,22 @@ class Route:
     @property
     def device(self):
         return self._buf.device
+
+    @classmethod
+    def pair(cls, T: int, cp: int, device=None):
+        """(z2c, c2z) routes in one buffer that share their common arrays
+        (thd_route_bind_pair): 16 bytes per row instead of 24, and the
+        two-direction build writes each shared array once."""
+        lib = L.load()
+        nbytes = lib.thd_route_pair_bytes(int(T), int(cp))
+        if nbytes == 0:
+            raise ThdError(L.ERR_INVALID_ARG, f"Route.pair(T={T}, cp={cp})")
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
+        zc, cz = L.ThdRoute(), L.ThdRoute()
+        _raise_host(lib.thd_route_bind_pair(ctypes.byref(zc), ctypes.byref(cz), buf.data_ptr(), nbytes, int(T),
+                                            int(cp)), "thd_route_bind_pair")
+        return (cls(T, cp, ZIGZAG_TO_CONTIGUOUS, _bound=(buf, zc)),
+                cls(T, cp, CONTIGUOUS_TO_ZIGZAG, _bound=(buf, cz)))
 
 
 def route_build(cu_seqlens_padded: torch.Tensor, T: int, cp: int, direction: int, status=None,
@@ -169,11 +188,12 @@ def route_build(cu_seqlens_padded: torch.Tensor, T: int, cp: int, direction: int
 
 def route_build_pair(cu_seqlens_padded: torch.Tensor, T: int, cp: int, status=None,
                      routes: tuple | None = None, stream=None):
-    """Build both directions' routes in one launch; returns (z2c, c2z)."""
+    """Build both directions' routes in one launch; returns (z2c, c2z).
+
+    Without ``routes`` the two share one buffer (Route.pair)."""
     _need_cuda(cu_seqlens_padded, "cu_seqlens_padded", torch.int32)
     if routes is None:
-        dev = cu_seqlens_padded.device
-        routes = (Route(T, cp, ZIGZAG_TO_CONTIGUOUS, dev), Route(T, cp, CONTIGUOUS_TO_ZIGZAG, dev))
+        routes = Route.pair(T, cp, cu_seqlens_padded.device)
     if status is None:
         status = new_status(cu_seqlens_padded.device)
     fwd, bwd = routes

@@ -105,6 +105,53 @@ thd_status_t thd_route_bind(thd_route_t* route, void* d_base, size_t bytes, int6
   return THD_OK;
 }
 
+size_t thd_route_pair_bytes(int64_t T, int32_t cp) {
+  if (!route_args_ok(T, cp)) return 0;
+  const size_t rows = static_cast<size_t>(T) * sizeof(int32_t);
+  const size_t sq = static_cast<size_t>(cp) * cp * sizeof(int32_t);
+  const size_t off = static_cast<size_t>(cp) * (cp + 1) * sizeof(int32_t);
+  const size_t flag = static_cast<size_t>(cp);
+  return 4 * align256(rows) + 2 * (2 * align256(sq) + 2 * align256(off) + 2 * align256(flag));
+}
+
+thd_status_t thd_route_bind_pair(thd_route_t* route_z2c, thd_route_t* route_c2z, void* d_base, size_t bytes,
+                                 int64_t T, int32_t cp) {
+  if (!route_z2c || !route_c2z || route_z2c == route_c2z) return THD_ERR_INVALID_ARG;
+  const size_t need = thd_route_pair_bytes(T, cp);
+  if (need == 0 || !d_base || bytes < need || reinterpret_cast<uintptr_t>(d_base) % 256 != 0)
+    return THD_ERR_INVALID_ARG;
+  char* p = static_cast<char*>(d_base);
+  auto take = [&p](size_t n) {
+    char* q = p;
+    p += align256(n);
+    return q;
+  };
+  const size_t rows = static_cast<size_t>(T) * sizeof(int32_t);
+  int32_t* zc_src = reinterpret_cast<int32_t*>(take(rows));
+  int32_t* cz_src = reinterpret_cast<int32_t*>(take(rows));
+  // z->c receive rows == c->z send rows; z->c send rows == c->z receive rows
+  // == 0..S-1 on every rank
+  int32_t* shared_rows = reinterpret_cast<int32_t*>(take(rows));
+  int32_t* in_order = reinterpret_cast<int32_t*>(take(rows));
+  thd_route_t* rt[2] = {route_z2c, route_c2z};
+  for (int k = 0; k < 2; ++k) {
+    thd_route_t* r = rt[k];
+    r->cp_size = cp;
+    r->dir = k == 0 ? THD_ZIGZAG_TO_CONTIGUOUS : THD_CONTIGUOUS_TO_ZIGZAG;
+    r->total_rows = T;
+    r->src_of_dst = k == 0 ? zc_src : cz_src;
+    r->send_rows = k == 0 ? in_order : shared_rows;
+    r->recv_rows = k == 0 ? shared_rows : in_order;
+    r->input_split_sizes = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cp) * cp * 4));
+    r->output_split_sizes = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cp) * cp * 4));
+    r->send_offsets = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cp) * (cp + 1) * 4));
+    r->recv_offsets = reinterpret_cast<int32_t*>(take(static_cast<size_t>(cp) * (cp + 1) * 4));
+    r->send_identity = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(cp)));
+    r->recv_identity = reinterpret_cast<uint8_t*>(take(static_cast<size_t>(cp)));
+  }
+  return THD_OK;
+}
+
 thd_status_t thd_route_build(const int32_t* cu_seqlens_padded, int32_t num_docs, int64_t T, int32_t cp_size,
                              thd_dir_t dir, const thd_route_t* route, int32_t* d_status,
                              cudaStream_t stream) {

@@ -23,7 +23,11 @@
 namespace thd {
 namespace {
 
-constexpr int kRouteThreads = 512;
+// Threads per block of the walking kernels (a sweep knob).
+#ifndef THD_ROUTE_THREADS
+#define THD_ROUTE_THREADS 512
+#endif
+constexpr int kRouteThreads = THD_ROUTE_THREADS;
 constexpr int kSmemBudget = 48 * 1024;
 // Launch shape of the walking kernels: at most this many blocks per SM (a
 // sweep on GB300 over 1-2 blocks per SM and 1-16 items per warp put one
@@ -47,6 +51,10 @@ struct RouteArgs {
   bool cu_in_smem;
   thd_route_t zc;  // zigzag -> contiguous (used when bit 0 of DIRS is set)
   thd_route_t cz;  // contiguous -> zigzag (used when bit 1 of DIRS is set)
+  // both directions: arrays that the two routes share (thd_route_bind_pair)
+  // are written once -- z->c receive rows are c->z send rows, and z->c send
+  // rows are c->z receive rows (0..S-1 on every rank)
+  bool cz_send_shared, cz_recv_shared;
   int32_t* status;
 };
 
@@ -113,7 +121,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   int32_t* cnt = smem;                        // [cp][cp+1]: zigzag rows of s below d*S
   int32_t* roff = cnt + cp * (cp + 1);        // [d][cp+1]: z->c receive offsets
   int32_t* bnd = roff + cp * (cp + 1);        // [3][cp+1]: document start, chunk, offset at d*S
-  int32_t* cu_s = bnd + 3 * (cp + 1);
+  int32_t* prd = bnd + 3 * (cp + 1);          // [r][d]: d*S + roff[d][r] - cnt[r][d]
+  int32_t* cu_s = prd + cp * cp;
   pdl_wait_then_release();
   const int32_t code = stage_check_cu(a.cu, n, cu_s, SMEM_CU, a.status, T, 2 * cp);
   if (code != THD_OK) {
@@ -161,6 +170,24 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
       roff[e] = p[0] - p[1];
     }
   }
+  // where rank r's rows bound for contiguous rank d start in d's receive
+  // buffer, less the zigzag rows of r below d*S: an entry's place is then
+  // prd[r][d] + its slot (the same closed forms as cnt and roff)
+  for (int32_t e = threadIdx.x; e < cp * cp; e += blockDim.x) {
+    const int32_t r = e / cp, d = e - r * cp;
+    int32_t c = bnd[(cp + 1) + d], off = bnd[2 * (cp + 1) + d];
+    const int32_t cnt_rd =
+        c < 0 ? S : m.div(bnd[d]) + min(max(off - r * c, 0), c) + min(max(off - (2 * cp - 1 - r) * c, 0), c);
+    int32_t p[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int32_t b = d + 1 - k;  // boundary X_{d+1}, then X_d
+      c = bnd[(cp + 1) + b];
+      off = bnd[2 * (cp + 1) + b];
+      p[k] = c < 0 ? r * S : r * m.div(bnd[b]) + min(off, r * c) + max(0, off - (2 * cp - r) * c);
+    }
+    prd[e] = d * S + (p[0] - p[1]) - cnt_rd;
+  }
   __syncthreads();
 
   // the last block has the fewest walk items (equal shares, remainder last)
@@ -194,7 +221,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
       const int32_t u = r * S + t.j;
       if (!in_range(g, 0, T, a.status)) continue;
       const int32_t d = divS.div(g);
-      const int32_t pos = d * S + roff[d * (cp + 1) + r] + (t.j - cnt[r * (cp + 1) + d]);
+      const int32_t pos = prd[r * cp + d] + t.j;
       if (!in_range(pos, d * static_cast<int64_t>(S), (d + 1) * static_cast<int64_t>(S), a.status)) continue;
       if (DIRS & kZC) {
         a.zc.src_of_dst[g] = u;
@@ -203,8 +230,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
       }
       if (DIRS & kCZ) {
         a.cz.src_of_dst[u] = g;
-        a.cz.recv_rows[u] = t.j;
-        a.cz.send_rows[pos] = g - d * S;
+        if (!(DIRS & kZC) || !a.cz_recv_shared) a.cz.recv_rows[u] = t.j;
+        if (!(DIRS & kZC) || !a.cz_send_shared) a.cz.send_rows[pos] = g - d * S;
       }
     }
   }
@@ -271,26 +298,30 @@ thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t
   a.zc = zc ? *zc : thd_route_t{};
   a.cz = cz ? *cz : thd_route_t{};
   a.status = status;
-  size_t tables = static_cast<size_t>(2 * cp + 3) * (cp + 1) * sizeof(int32_t);
-  size_t cu_bytes = static_cast<size_t>(n + 1) * sizeof(int32_t);
-  a.cu_in_smem = tables + cu_bytes <= static_cast<size_t>(kSmemBudget);
-  size_t smem = tables + (a.cu_in_smem ? cu_bytes : 0);
-  int grid = grid_for_items((static_cast<int64_t>(a.S) + 31) / 32 * cp);
+  a.cz_send_shared = zc && cz && zc->recv_rows == cz->send_rows;
+  a.cz_recv_shared = zc && cz && zc->send_rows == cz->recv_rows;
+  const size_t tables =
+      (static_cast<size_t>(2 * cp + 3) * (cp + 1) + static_cast<size_t>(cp) * cp) * sizeof(int32_t);
+  const size_t cu_bytes = static_cast<size_t>(n + 1) * sizeof(int32_t);
+  a.cu_in_smem = cu_bytes <= static_cast<size_t>(kSmemBudget);
+  const size_t smem = tables + (a.cu_in_smem ? cu_bytes : 0);
+  const int grid = grid_for_items((static_cast<int64_t>(a.S) + 31) / 32 * cp);
+  auto go = [&](void (*kernel)(RouteArgs)) -> cudaError_t {
+    // above 48 KB (cp near 64 with many documents) the block opts in to more
+    if (smem > 48 * 1024) {
+      const cudaError_t e0 =
+          cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+      if (e0 != cudaSuccess) return e0;
+    }
+    return launch_pdl(kernel, grid, kRouteThreads, smem, s, a);
+  };
   cudaError_t e;
   if (a.cu_in_smem) {
-    if (dirs == (kZC | kCZ))
-      e = launch_pdl(route_build_kernel<kZC | kCZ, true>, grid, kRouteThreads, smem, s, a);
-    else if (dirs == kZC)
-      e = launch_pdl(route_build_kernel<kZC, true>, grid, kRouteThreads, smem, s, a);
-    else
-      e = launch_pdl(route_build_kernel<kCZ, true>, grid, kRouteThreads, smem, s, a);
+    e = go(dirs == (kZC | kCZ) ? route_build_kernel<kZC | kCZ, true>
+                               : dirs == kZC ? route_build_kernel<kZC, true> : route_build_kernel<kCZ, true>);
   } else {
-    if (dirs == (kZC | kCZ))
-      e = launch_pdl(route_build_kernel<kZC | kCZ, false>, grid, kRouteThreads, smem, s, a);
-    else if (dirs == kZC)
-      e = launch_pdl(route_build_kernel<kZC, false>, grid, kRouteThreads, smem, s, a);
-    else
-      e = launch_pdl(route_build_kernel<kCZ, false>, grid, kRouteThreads, smem, s, a);
+    e = go(dirs == (kZC | kCZ) ? route_build_kernel<kZC | kCZ, false>
+                               : dirs == kZC ? route_build_kernel<kZC, false> : route_build_kernel<kCZ, false>);
   }
   if (e != cudaSuccess) {
     record_cuda_error(e);

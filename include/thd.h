@@ -129,6 +129,23 @@ thd_status_t thd_route_bind(thd_route_t *route, void *d_base, size_t bytes,
                             int64_t T, int32_t cp, thd_dir_t dir);
 
 /*
+ * Both directions' routes for the same T and cp in ONE caller buffer of
+ * thd_route_pair_bytes(T, cp) bytes (256-byte aligned), sharing the arrays
+ * whose contents the two directions have in common: route_c2z->send_rows is
+ * route_z2c->recv_rows (the rows each contiguous rank receives from the
+ * zigzag ranks are the rows it sends back), and route_c2z->recv_rows is
+ * route_z2c->send_rows (0..S-1 on every rank: each rank's zigzag rows ascend
+ * in global order).  16 bytes per row for the pair instead of 24, and
+ * thd_route_build_pair writes each shared array once.  Every array of both
+ * routes stays complete and valid for every other call; building one
+ * direction alone into a pair-bound route writes the shared arrays with the
+ * same contents.  Host only: enqueues nothing.
+ */
+size_t thd_route_pair_bytes(int64_t T, int32_t cp);
+thd_status_t thd_route_bind_pair(thd_route_t *route_z2c, thd_route_t *route_c2z, void *d_base,
+                                 size_t bytes, int64_t T, int32_t cp);
+
+/*
  * Build the route of one direction on the device, with no host
  * synchronisation (Relax PR #273, section 2.1: route from cu_seqlens and
  * cp_size by interval intersection; section 2.3: fail-fast validation).

@@ -28,21 +28,34 @@ def _gpu_route(cu, T, cp, direction):
     return r
 
 
-def _gpu_pair(cu, T, cp):
+def _gpu_pair(cu, T, cp, shared=True):
+    """Both directions in one launch, into one buffer whose common arrays the
+    routes share (Route.pair) or into two separately bound routes."""
     st = thd.new_status()
-    f, b = thd.route_build_pair(_cu_tensor(cu), T, cp, status=st)
+    routes = None if shared else (thd.Route(T, cp, Z2C), thd.Route(T, cp, C2Z))
+    f, b = thd.route_build_pair(_cu_tensor(cu), T, cp, status=st, routes=routes)
     thd.check_status(st, "route_build_pair")
     return f, b
 
 
 def _assert_both(cu, T, cp):
-    """Each direction alone and both in one launch, against the oracle."""
+    """Each direction alone, and both in one launch into a shared and into
+    separate buffers, against the oracle; each direction alone into a
+    pair-bound buffer leaves the other direction's route intact."""
     want = [oracle.build_route(cu, T, cp, d) for d in (Z2C, C2Z)]
     for d in (Z2C, C2Z):
         _assert_route(_gpu_route(cu, T, cp, d), want[d])
-    f, b = _gpu_pair(cu, T, cp)
-    _assert_route(f, want[Z2C])
-    _assert_route(b, want[C2Z])
+    for shared in (True, False):
+        f, b = _gpu_pair(cu, T, cp, shared)
+        _assert_route(f, want[Z2C])
+        _assert_route(b, want[C2Z])
+    st = thd.new_status()
+    pf, pb = thd.Route.pair(T, cp)
+    thd.route_build(_cu_tensor(cu), T, cp, Z2C, status=st, route=pf)
+    thd.route_build(_cu_tensor(cu), T, cp, C2Z, status=st, route=pb)
+    thd.check_status(st)
+    _assert_route(pf, want[Z2C])
+    _assert_route(pb, want[C2Z])
     return want
 
 
