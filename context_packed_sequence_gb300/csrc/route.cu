@@ -48,6 +48,7 @@ struct RouteArgs {
   int32_t n, T, S;
   CpMath m;
   FastDiv divS;
+  FastDiv divCp1;  // by cp + 1
   bool cu_in_smem;
   thd_route_t zc;  // zigzag -> contiguous (used when bit 0 of DIRS is set)
   thd_route_t cz;  // contiguous -> zigzag (used when bit 1 of DIRS is set)
@@ -140,20 +141,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   //   with P(s, X) = rows of ranks < s below X
   //              = s*c0/cp + min(off, s*c) + max(0, off - (2cp-s)*c)
   //   (ranks below s own chunks [0, s) and [2cp-s, 2cp) of every document).
-  for (int32_t d = threadIdx.x; d <= cp; d += blockDim.x) {
+  // one warp per boundary, searching together
+  for (int32_t d = threadIdx.x >> 5; d <= cp; d += blockDim.x >> 5) {
     const int32_t X = d * S;
-    if (X >= T) {
-      bnd[d] = 0, bnd[(cp + 1) + d] = -1, bnd[2 * (cp + 1) + d] = 0;
-    } else {
-      const int32_t i = doc_of(cu, n, X);
-      bnd[d] = cu[i];
-      bnd[(cp + 1) + d] = m.div2(cu[i + 1] - cu[i]);
-      bnd[2 * (cp + 1) + d] = X - cu[i];
+    const int32_t i = X >= T ? 0 : warp_doc_of(cu, n, X);
+    if ((threadIdx.x & 31) == 0) {
+      if (X >= T) {
+        bnd[d] = 0, bnd[(cp + 1) + d] = -1, bnd[2 * (cp + 1) + d] = 0;
+      } else {
+        bnd[d] = cu[i];
+        bnd[(cp + 1) + d] = m.div2(cu[i + 1] - cu[i]);
+        bnd[2 * (cp + 1) + d] = X - cu[i];
+      }
     }
   }
   __syncthreads();
   for (int32_t e = threadIdx.x; e < cp * (cp + 1); e += blockDim.x) {
-    const int32_t x = e / (cp + 1), y = e - x * (cp + 1);
+    const int32_t x = a.divCp1.div(e), y = e - x * (cp + 1);
     {  // cnt[s = x][d = y]
       const int32_t c = bnd[(cp + 1) + y], off = bnd[2 * (cp + 1) + y];
       cnt[e] = c < 0 ? S
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   // buffer, less the zigzag rows of r below d*S: an entry's place is then
   // prd[r][d] + its slot (the same closed forms as cnt and roff)
   for (int32_t e = threadIdx.x; e < cp * cp; e += blockDim.x) {
-    const int32_t r = e / cp, d = e - r * cp;
+    const int32_t r = m.div(e), d = e - r * cp;
     int32_t c = bnd[(cp + 1) + d], off = bnd[2 * (cp + 1) + d];
     const int32_t cnt_rd =
         c < 0 ? S : m.div(bnd[d]) + min(max(off - r * c, 0), c) + min(max(off - (2 * cp - 1 - r) * c, 0), c);
@@ -190,12 +194,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   }
   __syncthreads();
 
-  // the last block has the fewest walk items (equal shares, remainder last)
-  if (blockIdx.x == gridDim.x - 1) {
-    if (DIRS & kZC) write_small_arrays(a.zc, true, cu, n, m, S, cnt, roff);
-    if (DIRS & kCZ) write_small_arrays(a.cz, false, cu, n, m, S, cnt, roff);
-  }
-
   // Zigzag position u = r*S + j holds global row g.  Then
   //   z->c: src_of_dst[g] = u, send_rows[u] = j;
   //   c->z: src_of_dst[u] = g, recv_rows[u] = j;
@@ -205,35 +203,53 @@ __global__ void __launch_bounds__(kRouteThreads) route_build_kernel(RouteArgs a)
   const int64_t tiles = (static_cast<int64_t>(S) + 31) / 32;
   int64_t begin, end;
   warp_items(tiles * cp, 1, &begin, &end);
-  if (begin >= end) return;
-  const FastDiv divS = a.divS;
-  int32_t wdoc = -1;
-  const int32_t t_last = static_cast<int32_t>((end - 1) / cp);
-  for (int32_t tile = static_cast<int32_t>(begin / cp); tile <= t_last; ++tile) {
-    const SlotTile t = slot_tile(cu, n, m, S, tile, wdoc);
-    const int64_t q0 = static_cast<int64_t>(tile) * cp;
-    const int32_t r0 = static_cast<int32_t>(max(begin - q0, int64_t{0}));
-    const int32_t r1 = static_cast<int32_t>(min(end - q0, static_cast<int64_t>(cp)));
-    if (!t.valid || !in_range(t.doc, 0, n, a.status)) continue;
+  if (begin < end) {
+    const FastDiv divS = a.divS;
+    // shared arrays are written once (both directions, pair-bound routes)
+    const bool w_recv = !(DIRS & kZC) || !a.cz_recv_shared;
+    const bool w_send = !(DIRS & kZC) || !a.cz_send_shared;
+    int32_t wdoc = -1;
+    const int32_t t_last = static_cast<int32_t>((end - 1) / cp);
+    for (int32_t tile = static_cast<int32_t>(begin / cp); tile <= t_last; ++tile) {
+      const SlotTile t = slot_tile(cu, n, m, S, tile, wdoc);
+      const int64_t q0 = static_cast<int64_t>(tile) * cp;
+      const int32_t r0 = static_cast<int32_t>(max(begin - q0, int64_t{0}));
+      const int32_t r1 = static_cast<int32_t>(min(end - q0, static_cast<int64_t>(cp)));
+      // A document inside one contiguous rank's interval (all but the few
+      // that straddle a boundary d*S) sends all its rows to the same rank
+      // d: then d is taken once for the lane instead of once per rank.
+      const int32_t d_lo = divS.div(t.c0), d_hi = divS.div(t.c1 - 1);
+      const bool one_d = __all_sync(kFullMask, !t.valid || d_lo == d_hi);
+      if (!t.valid || !in_range(t.doc, 0, n, a.status)) continue;
+      // rank r0's global row and zigzag position, then one rank further per step
+      int32_t g = t.base + r0 * t.step;
+      int32_t u = r0 * S + t.j;
+      const int32_t* prow = prd + r0 * cp;
 #pragma unroll kRouteUnroll
-    for (int32_t r = r0; r < r1; ++r) {
-      const int32_t g = t.base + r * t.step;
-      const int32_t u = r * S + t.j;
-      if (!in_range(g, 0, T, a.status)) continue;
-      const int32_t d = divS.div(g);
-      const int32_t pos = prd[r * cp + d] + t.j;
-      if (!in_range(pos, d * static_cast<int64_t>(S), (d + 1) * static_cast<int64_t>(S), a.status)) continue;
-      if (DIRS & kZC) {
-        a.zc.src_of_dst[g] = u;
-        a.zc.send_rows[u] = t.j;
-        a.zc.recv_rows[pos] = g - d * S;
-      }
-      if (DIRS & kCZ) {
-        a.cz.src_of_dst[u] = g;
-        if (!(DIRS & kZC) || !a.cz_recv_shared) a.cz.recv_rows[u] = t.j;
-        if (!(DIRS & kZC) || !a.cz_send_shared) a.cz.send_rows[pos] = g - d * S;
+      for (int32_t r = r0; r < r1; ++r, g += t.step, u += S, prow += cp) {
+        if (!in_range(g, 0, T, a.status)) continue;
+        const int32_t d = one_d ? d_lo : divS.div(g);
+        const int32_t pos = prow[d] + t.j;
+        const int32_t gl = g - d * S;
+        if (!in_range(pos, d * static_cast<int64_t>(S), (d + 1) * static_cast<int64_t>(S), a.status)) continue;
+        if (DIRS & kZC) {
+          a.zc.src_of_dst[g] = u;
+          a.zc.send_rows[u] = t.j;
+          a.zc.recv_rows[pos] = gl;
+        }
+        if (DIRS & kCZ) {
+          a.cz.src_of_dst[u] = g;
+          if (w_recv) a.cz.recv_rows[u] = t.j;
+          if (w_send) a.cz.send_rows[pos] = gl;
+        }
       }
     }
+  }
+  // split sizes, offsets and identity flags: the last block, which has the
+  // fewest walk items (equal shares, remainder last), after its walk
+  if (blockIdx.x == gridDim.x - 1) {
+    if (DIRS & kZC) write_small_arrays(a.zc, true, cu, n, m, S, cnt, roff);
+    if (DIRS & kCZ) write_small_arrays(a.cz, false, cu, n, m, S, cnt, roff);
   }
 }
 
@@ -295,6 +311,7 @@ thd_status_t launch_route_build(const int32_t* cu, int32_t n, int32_t T, int32_t
   a.S = T / cp;
   a.m = make_cp_math(cp);
   a.divS = make_fast_div(a.S > 0 ? a.S : 1);
+  a.divCp1 = make_fast_div(cp + 1);
   a.zc = zc ? *zc : thd_route_t{};
   a.cz = cz ? *cz : thd_route_t{};
   a.status = status;

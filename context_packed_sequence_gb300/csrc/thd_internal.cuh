@@ -250,6 +250,26 @@ __device__ __forceinline__ int32_t doc_in(const int32_t* cu, int32_t lo, int32_t
   return lo;
 }
 
+// Largest i in [0, n] with cu[i] <= x, given cu[0] <= x, by the whole warp
+// (every lane calls it with the same x): each round the lanes test 32
+// evenly spaced candidates of the bracket and the last one that passes
+// narrows it, so n + 1 = 4097 boundaries take 3 rounds instead of 12 halvings.
+// cu non-decreasing makes the passing candidates a prefix of the lanes.
+__device__ __forceinline__ int32_t warp_doc_of(const int32_t* cu, int32_t n, int32_t x) {
+  const int32_t lane = threadIdx.x & 31;
+  int32_t lo = 0, len = n + 1;  // the answer lies in [lo, lo + len)
+  while (len > 1) {
+    const int32_t stride = (len + 31) >> 5;
+    const int32_t off = lane * stride;
+    const bool ok = off < len && cu[lo + off] <= x;
+    const uint32_t b = __ballot_sync(kFullMask, ok);  // bit 0 set: cu[lo] <= x
+    const int32_t k = 31 - __clz(b);
+    lo += k * stride;
+    len = min(stride, len - k * stride);
+  }
+  return lo;
+}
+
 // Largest k >= i with cu[k] <= x, given cu[i] <= x: gallop forward from i
 // (1, 2, 4, ... documents), then search the last bracket.  Costs O(log of the
 // distance), so following a position that only moves forward is cheap.
@@ -284,6 +304,7 @@ struct SlotTile {
   bool valid;          // the lane's slot is below S (clamped lanes must not store)
   int32_t doc;         // document holding slot j
   int32_t base, step;  // rank r's global row: base + r*step
+  int32_t c0, c1;      // the document's rows [c0, c1)
 };
 
 // Documents of the slots of tile `tile` (every lane of the warp calls it
@@ -300,15 +321,17 @@ __device__ __forceinline__ SlotTile slot_tile(const int32_t* cu, int32_t n, CpMa
   t.valid = lane <= left;
   t.j = j0 + min(lane, left);
   const int32_t x_lo = j0 * m.cp, x_hi = (j0 + min(31, left)) * m.cp;
-  const int32_t i_lo = wdoc < 0 ? doc_of(cu, n, x_lo) : doc_from(cu, n, wdoc, x_lo);
+  const int32_t i_lo = wdoc < 0 ? warp_doc_of(cu, n, x_lo) : doc_from(cu, n, wdoc, x_lo);
   const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
   wdoc = i_lo;
   const int32_t i = doc_in(cu, i_lo, i_hi, t.j * m.cp);
-  const int32_t c0 = cu[i];
-  const int32_t c = m.div2(cu[i + 1] - c0);
+  const int32_t c0 = cu[i], c1 = cu[i + 1];
+  const int32_t c = m.div2(c1 - c0);
   const int32_t loc = t.j - m.div(c0);
   const bool front = loc < c;
   t.doc = i;
+  t.c0 = c0;
+  t.c1 = c1;
   t.base = front ? c0 + loc : c0 + (2 * m.cp - 2) * c + loc;
   t.step = front ? c : -c;
   return t;
