@@ -10,15 +10,30 @@
 // end e_i, else `fill` with mask 0.  Warps walk contiguous position ranges
 // and follow the current document forward, so finding it costs a step or
 // two per 32 positions instead of a full search per position; the zigzag
-// variant walks slot tiles shared by every rank, as the route build does.
+// variant walks the rows the same way and writes each to its zigzag slot.
 #include "thd_internal.cuh"
 
 namespace thd {
 namespace {
 
 constexpr int kLabelThreads = 512;
-constexpr int kSmemBudget = 48 * 1024;
-// At most this many blocks per SM for the zigzag variant's slot-tile walk.
+// Boundaries (padded and unpadded) staged in shared memory up to this size
+// (about 20,000 documents); above 48 KB the launch opts in to the larger
+// dynamic shared memory.  Searching them in global memory instead puts an L2
+// round trip on every step of every warp's document search.
+constexpr int kSmemBudget = 160 * 1024;
+
+// Launch with `smem` bytes of dynamic shared memory, opting in above 48 KB.
+template <typename... Params, typename... Args>
+cudaError_t launch_smem(void (*kernel)(Params...), dim3 grid, size_t smem, cudaStream_t s, Args... args) {
+  if (smem > 48 * 1024) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(kernel, grid, dim3(kLabelThreads), smem, s, args...);
+}
+// At most this many blocks per SM for the zigzag variant.
 #ifndef THD_LABEL_ZZ_BLOCKS_PER_SM
 #define THD_LABEL_ZZ_BLOCKS_PER_SM 2
 #endif
@@ -30,32 +45,6 @@ struct NextTokens {
   const int32_t* tok;
   const uint8_t* has;
 };
-
-// Targets of global row g (document i, valid end e) written at position out:
-// depth k takes tokens[g+1+k] while inside the document, the document's next
-// token exactly one past its end, else `fill` with mask 0.
-__device__ __forceinline__ void write_targets(const int32_t* __restrict__ tokens, NextTokens next, int32_t i,
-                                              int32_t g, int32_t out, int32_t e, int32_t depth, int32_t fill,
-                                              int32_t T, int32_t* __restrict__ labels,
-                                              uint8_t* __restrict__ lmask) {
-  const bool cont = next.has != nullptr && next.has[i] != 0;
-  // depth k reads tokens[g+1+k] while k < room; comparing k with the room left
-  // keeps every sum below e, so nothing overflows when T is near INT32_MAX
-  const int32_t room = e - g - 1;
-  for (int32_t k = 0; k <= depth; ++k) {
-    int32_t v = fill;
-    uint8_t ok = 0;
-    if (k < room) {
-      v = __ldg(tokens + g + 1 + k);
-      ok = 1;
-    } else if (k == room && cont) {
-      v = next.tok[i];
-      ok = 1;
-    }
-    labels[static_cast<int64_t>(k) * T + out] = v;
-    lmask[static_cast<int64_t>(k) * T + out] = ok;
-  }
-}
 
 // Positions per lane: a lane writes each depth's four labels with one
 // 16-byte store and its four masks with one 4-byte store (VEC: T a multiple
@@ -169,9 +158,14 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
   }
 }
 
-// The same labels written in the zigzag layout: position p = r*S + j of the
-// zigzag buffer holds global row g, so out[k][p] = labels[k][g] (and the same
-// for the masks) -- the label roll and the partition gather in one pass.
+// The same labels written in the zigzag layout: global row g goes to zigzag
+// position u = r*S + j, so out[k][u] = labels[k][g] (and the same for the
+// masks) -- the label roll and the partition gather in one pass.  Warps walk
+// global rows in order, following the current document forward as the
+// contiguous kernel does, so every token is read once and in order; row g of document i (start c0, chunk length c) lies in chunk
+// k = (g - c0) / c, which rank r = k or 2cp-1-k holds at local slot
+// c0/cp + (k < cp ? 0 : c) + (g - c0 - k*c).  The writes follow the zigzag
+// order in runs of one chunk.
 template <bool SMEM_CU>
 __global__ void __launch_bounds__(kLabelThreads)
 roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
@@ -200,29 +194,67 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
     if (blockIdx.x == 0 && threadIdx.x == 0) status_set(status, code);
     return;
   }
-  // (slot tile, rank) items as in the route build: a tile's documents and
-  // valid ends are found once and serve every rank's row of each slot
+  if (T == 0) return;
   const int32_t S = T / m.cp;
-  const int64_t tiles = (static_cast<int64_t>(S) + 31) / 32;
-  int64_t begin, end;
-  warp_items(tiles * m.cp, 1, &begin, &end);
-  if (begin >= end) return;
-  int32_t wdoc = -1;
-  const int32_t t_last = static_cast<int32_t>((end - 1) / m.cp);
-  for (int32_t tile = static_cast<int32_t>(begin / m.cp); tile <= t_last; ++tile) {
-    const SlotTile t = slot_tile(cu, n, m, S, tile, wdoc);
-    const int64_t q0 = static_cast<int64_t>(tile) * m.cp;
-    const int32_t r0 = static_cast<int32_t>(max(begin - q0, int64_t{0}));
-    const int32_t r1 = static_cast<int32_t>(min(end - q0, static_cast<int64_t>(m.cp)));
-    if (!t.valid || !in_range(t.doc, 0, n, status)) continue;
-    const int32_t e = cu[t.doc] + (cu_v[t.doc + 1] - cu_v[t.doc]);  // end of the document's valid tokens
-    if (!in_range(e, 0, static_cast<int64_t>(T) + 1, status)) continue;  // token reads stay below e
-    for (int32_t r = r0; r < r1; ++r) {
-      const int32_t g = t.base + r * t.step;
-      const int32_t u = r * S + t.j;
-      if (!in_range(g, 0, T, status)) continue;
-      valid[u] = g < e ? 1 : 0;
-      write_targets(tokens, next, t.doc, g, u, e, depth, fill, T, labels, lmask);
+  // Each warp an equal contiguous range of rows, 128 per step: four groups of
+  // 32 consecutive rows, one row of each per lane, so every depth issues four
+  // independent token loads per lane.  Steps start at multiples of 128, so
+  // g stays within int32 for every T below 2^31.
+  constexpr int kGroups = 4;
+  constexpr int kStep = 32 * kGroups;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t steps = (static_cast<int64_t>(T) + kStep - 1) / kStep;
+  const int64_t per = (steps + nwarps - 1) / nwarps;
+  const int64_t begin = min(static_cast<int64_t>(T), warp * per * kStep);
+  const int64_t end = min(static_cast<int64_t>(T), (warp + 1) * per * kStep);
+  const int32_t lane = threadIdx.x & 31;
+  const int32_t last = static_cast<int32_t>(end) - 1;
+  const bool has_next = next.has != nullptr;
+  int32_t doc = -1;
+  for (int64_t step0 = begin; step0 < end; step0 += kStep) {
+    const int32_t x_lo = static_cast<int32_t>(step0);
+    const int32_t x_hi = min(x_lo + kStep - 1, last);
+    const int32_t i_lo = doc < 0 ? doc_of(cu, n, x_lo) : doc_from(cu, n, doc, x_lo);
+    const int32_t i_hi = doc_from(cu, n, i_lo, x_hi);
+    doc = i_lo;
+    int32_t gq[kGroups], uq[kGroups], room[kGroups], iq[kGroups];
+    bool ok[kGroups];
+    int32_t i = i_lo;
+#pragma unroll
+    for (int q = 0; q < kGroups; ++q) {
+      const int32_t g = x_lo + 32 * q + lane;
+      i = doc_in(cu, i, i_hi, min(g, last));  // rows only move forward
+      const int32_t c0 = cu[i];
+      const int32_t c = m.div2(cu[i + 1] - c0);  // >= 1: document i holds row min(g, last)
+      const int32_t off = min(g, last) - c0;
+      const int32_t k = off / c;                 // chunk 0 .. 2cp-1
+      const bool front = k < m.cp;
+      const int32_t u = (front ? k : 2 * m.cp - 1 - k) * S + m.div(c0) + (front ? 0 : c) + (off - k * c);
+      const int32_t e = c0 + (cu_v[i + 1] - cu_v[i]);  // end of the document's valid tokens
+      ok[q] = g <= last && in_range(i, 0, n, status) && in_range(u, 0, T, status) &&
+              in_range(e, 0, static_cast<int64_t>(T) + 1, status);
+      gq[q] = g;
+      uq[q] = u;
+      iq[q] = i;
+      room[q] = e - g - 1;  // depth k reads tokens[g+1+k] while k < room (no sum passes e)
+      if (ok[q]) valid[u] = g < e ? 1 : 0;
+    }
+    for (int32_t k = 0; k <= depth; ++k) {
+      int32_t v[kGroups];
+#pragma unroll
+      for (int q = 0; q < kGroups; ++q) v[q] = ok[q] && k < room[q] ? __ldg(tokens + gq[q] + 1 + k) : fill;
+#pragma unroll
+      for (int q = 0; q < kGroups; ++q) {
+        if (!ok[q]) continue;
+        uint8_t mk = k < room[q] ? 1 : 0;
+        if (k == room[q] && has_next && next.has[iq[q]] != 0) {  // the document's next token, one past its end
+          v[q] = next.tok[iq[q]];
+          mk = 1;
+        }
+        labels[static_cast<int64_t>(k) * T + uq[q]] = v[q];
+        lmask[static_cast<int64_t>(k) * T + uq[q]] = mk;
+      }
     }
   }
 }
@@ -236,17 +268,17 @@ thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_
   const NextTokens next{next_tok, has_next};
   size_t bytes = static_cast<size_t>(2) * (n + 1) * sizeof(int32_t);
   bool in_smem = bytes <= static_cast<size_t>(kSmemBudget);
-  int64_t grid = (static_cast<int64_t>(T) + kLabelThreads - 1) / kLabelThreads;
+  int64_t grid = (static_cast<int64_t>(T) + 4 * kLabelThreads - 1) / (4 * kLabelThreads);  // four rows per thread
   int64_t cap = static_cast<int64_t>(sm_count()) * THD_LABEL_ZZ_BLOCKS_PER_SM;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   const CpMath m = make_cp_math(cp);
   const dim3 blocks(static_cast<unsigned>(grid));
   const cudaError_t e =
-      in_smem ? launch_pdl(roll_labels_zigzag_kernel<true>, blocks, kLabelThreads, bytes, s, tokens, cu_v, cu, n, T,
-                           m, depth, fill, next, labels, lmask, valid, status)
-              : launch_pdl(roll_labels_zigzag_kernel<false>, blocks, kLabelThreads, 0, s, tokens, cu_v, cu, n, T, m,
-                           depth, fill, next, labels, lmask, valid, status);
+      in_smem ? launch_smem(roll_labels_zigzag_kernel<true>, blocks, bytes, s, tokens, cu_v, cu, n, T, m, depth, fill,
+                            next, labels, lmask, valid, status)
+              : launch_smem(roll_labels_zigzag_kernel<false>, blocks, 0, s, tokens, cu_v, cu, n, T, m, depth, fill,
+                            next, labels, lmask, valid, status);
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
@@ -271,14 +303,14 @@ thd_status_t launch_roll_labels(const int32_t* tokens, const int32_t* cu_v, cons
                    reinterpret_cast<uintptr_t>(lmask) % 4 == 0 && reinterpret_cast<uintptr_t>(valid) % 4 == 0;
   const size_t smem = in_smem ? bytes : 0;
   const cudaError_t e =
-      vec ? (in_smem ? launch_pdl(roll_labels_kernel<true, true>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu, n,
-                                  T, depth, fill, next, labels, lmask, valid, status)
-                     : launch_pdl(roll_labels_kernel<false, true>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu, n,
-                                  T, depth, fill, next, labels, lmask, valid, status))
-          : (in_smem ? launch_pdl(roll_labels_kernel<true, false>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu,
-                                  n, T, depth, fill, next, labels, lmask, valid, status)
-                     : launch_pdl(roll_labels_kernel<false, false>, blocks, kLabelThreads, smem, s, tokens, cu_v, cu,
-                                  n, T, depth, fill, next, labels, lmask, valid, status));
+      vec ? (in_smem ? launch_smem(roll_labels_kernel<true, true>, blocks, smem, s, tokens, cu_v, cu, n, T, depth,
+                                   fill, next, labels, lmask, valid, status)
+                     : launch_smem(roll_labels_kernel<false, true>, blocks, smem, s, tokens, cu_v, cu, n, T, depth,
+                                   fill, next, labels, lmask, valid, status))
+          : (in_smem ? launch_smem(roll_labels_kernel<true, false>, blocks, smem, s, tokens, cu_v, cu, n, T, depth,
+                                   fill, next, labels, lmask, valid, status)
+                     : launch_smem(roll_labels_kernel<false, false>, blocks, smem, s, tokens, cu_v, cu, n, T, depth,
+                                   fill, next, labels, lmask, valid, status));
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;

@@ -499,14 +499,15 @@ def test_roll_labels_zigzag_parity(cp, depth):
         assert got[2].cpu().tolist() == want[2]
 
 
-@pytest.mark.parametrize("cp", [1, 4])
-def test_labels_and_partition_beyond_shared_memory(cp):
-    """13,000 documents (empty ones included): the label kernels and the
-    partition kernel search the boundaries in global memory instead of
-    shared memory.  Labels with MTP depth 2 and per-document extra tokens,
-    in both layouts, and the partition of every rank, against the oracle."""
-    rng = np.random.default_rng(123 + cp)
-    n = 13000
+@pytest.mark.parametrize("cp,n", [(1, 13000), (4, 13000), (4, 24000)])
+def test_labels_and_partition_beyond_shared_memory(cp, n):
+    """Many documents (empty ones included): with 13,000 the label kernels
+    stage both boundary arrays (104 KB) in shared memory above the default
+    48 KB and the partition kernel searches global memory; with 24,000 (192
+    KB) the label kernels search global memory too.  Labels with MTP depth 2
+    and per-document extra tokens, in both layouts, and the partition of
+    every rank, against the oracle."""
+    rng = np.random.default_rng(123 + cp + n)
     lp = [2 * cp * int(rng.integers(0, 4)) for _ in range(n)]
     lv = [min(L, int(rng.integers(0, L + 3))) if L else 0 for L in lp]
     cu_v, cu = _bounds(lv), _bounds(lp)
