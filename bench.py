@@ -632,9 +632,10 @@ def run_thd(args, rank, world, local):
         e2e = run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes,
                       steps=max(12, args.steps))
 
-    others = None
+    others = prep_scale = None
     if not args.no_other_configs:
         others = run_other_configs(thd, lib, w.name, device, stream, status)
+        prep_scale = run_prep_at_scale(thd, lib, device, stream, status)
 
     peak, peak_kind = measured_peak()
     traffic = swap_traffic_record(w.name)
@@ -697,6 +698,8 @@ def run_thd(args, rank, world, local):
         result["swap_steady_state"] = steady
     if others:
         result["other_configs"] = others
+    if prep_scale:
+        result["data_prep_at_scale"] = prep_scale
     return result, dict(x=x, T=T, cu=cu_d, w=w, row_bytes=row_bytes)
 
 
@@ -864,6 +867,65 @@ def run_e2e(thd, w, x, T, cp, cu_d, row_bytes, layers, device, world, swap_bytes
             "overlap": f"uploads ({ahead} steps ahead) and downloads on two copy streams, {slots} buffer slots, "
                        "against compute; slot reuse waits on the host",
             "link_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs}}
+
+
+def run_prep_at_scale(thd, lib, device, stream, status, B=64, S=262144, cp=8, depth=3):
+    """The data-preparation kernels on 64 raw rows of 262,144 tokens (16.8 M,
+    drawn like the pipeline workload's rows), where launch latency no longer
+    hides them: packing, labels with three MTP depths in both layouts, and
+    the partition of every rank.  Each: launches back to back between CUDA
+    events, per launch, median; bytes per launch are the algorithmic ones
+    (packing: raw tokens read + packed tokens and boundaries written; labels:
+    tokens read + (depth + 1) x (4 + 1) bytes + 1 valid byte written per
+    position; partition: 4 bytes written per position)."""
+    import ctypes
+
+    peak_gbs, peak_kind = measured_peak()
+    sp = stream.cuda_stream
+    raw = torch.from_numpy(W.raw_pipeline_tokens(W.SEED + 4, B=B, S=S)).to(device)
+    tok, cu_v, cu = thd.pack_docs(raw, W.EOD_ID, 2 * cp, pad_id=0)
+    T, n = tok.numel(), cu.numel() - 1
+    cap_tok, cap_docs = B * S * 2 * cp, B * S + 1
+    ptok = torch.empty(cap_tok, dtype=torch.int32, device=device)
+    pcu_v = torch.empty(cap_docs, dtype=torch.int32, device=device)
+    pcu = torch.empty(cap_docs, dtype=torch.int32, device=device)
+    counts = torch.zeros(2, dtype=torch.int64, device=device)
+    ws = torch.empty(lib.thd_pack_docs_workspace_bytes(B, S), dtype=torch.uint8, device=device)
+    labels = torch.empty((depth + 1, T), dtype=torch.int32, device=device)
+    lmask = torch.empty((depth + 1, T), dtype=torch.uint8, device=device)
+    valid = torch.empty((T,), dtype=torch.uint8, device=device)
+    pidx = torch.empty((cp, T // cp), dtype=torch.int32, device=device)
+    calls = {
+        "pack_docs": (lambda: lib.thd_pack_docs(raw.data_ptr(), B, S, W.EOD_ID, 0, 0, 2 * cp, 0, None, ptok.data_ptr(),
+                                                cap_tok, pcu_v.data_ptr(), pcu.data_ptr(), None, None, cap_docs,
+                                                counts.data_ptr(), ws.data_ptr(), ws.numel(), status.data_ptr(), sp),
+                      4 * B * S + 4 * T + 8 * (n + 1)),
+        "roll_labels": (lambda: lib.thd_roll_labels(tok.data_ptr(), cu_v.data_ptr(), cu.data_ptr(), n, T, depth, 0, None,
+                                                    None, labels.data_ptr(), lmask.data_ptr(), valid.data_ptr(),
+                                                    status.data_ptr(), sp),
+                        4 * T + (depth + 1) * 5 * T + T),
+        "roll_labels_zigzag": (lambda: lib.thd_roll_labels_zigzag(tok.data_ptr(), cu_v.data_ptr(), cu.data_ptr(), n, T,
+                                                                  cp, depth, 0, None, None, labels.data_ptr(),
+                                                                  lmask.data_ptr(), valid.data_ptr(), status.data_ptr(),
+                                                                  sp),
+                               4 * T + (depth + 1) * 5 * T + T),
+        "partition": (lambda: lib.thd_partition_indices(cu.data_ptr(), n, T, cp, -1, pidx.data_ptr(), status.data_ptr(),
+                                                        sp),
+                      4 * T),
+    }
+    out = {"raw_rows": [B, S], "T": T, "num_docs": n, "cp_size": cp, "mtp_depth": depth,
+           "method": "3 launches back to back between CUDA events, per launch, median of 6; peak = "
+                     f"{peak_kind} copy bandwidth {peak_gbs} GB/s"}
+    for name, (fn, nbytes) in calls.items():
+        us = back_to_back_us(fn, stream, device, launches=3, reps=8, skip=2)
+        out[name] = {"us": us, "algorithmic_bytes": int(nbytes), "gbs": round(nbytes / us / 1e3, 1),
+                     "frac_of_measured": round(nbytes / us / 1e3 / peak_gbs, 4)}
+    torch.cuda.synchronize(device)
+    if thd.status_read(status) != 0:
+        raise RuntimeError("device status set by the data-preparation kernels at scale")
+    del raw, ptok, labels, lmask, valid, pidx, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_cp_exchange(args, rank, world, local):
