@@ -166,7 +166,18 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
 // k = (g - c0) / c, which rank r = k or 2cp-1-k holds at local slot
 // c0/cp + (k < cp ? 0 : c) + (g - c0 - k*c).  The writes follow the zigzag
 // order in runs of one chunk.
-template <bool SMEM_CU>
+// floor(off / c) for 0 <= off and 1 <= c: below 2^24 both are exact in
+// float, the float quotient is within one of the true one, and one
+// integer step on each side corrects it; larger offsets divide exactly.
+__device__ __forceinline__ int32_t chunk_of(int32_t off, int32_t c) {
+  if (off >= (1 << 24)) return off / c;
+  int32_t k = __float2int_rz(__fdividef(static_cast<float>(off), static_cast<float>(c)));
+  if (k * c > off) --k;
+  else if ((k + 1) * c <= off) ++k;
+  return k;
+}
+
+template <bool SMEM_CU, bool NEXT>
 __global__ void __launch_bounds__(kLabelThreads)
 roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, const int32_t* cu_g,
                           int32_t n, int32_t T, CpMath m, int32_t depth, int32_t fill, NextTokens next,
@@ -210,7 +221,6 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
   const int64_t end = min(static_cast<int64_t>(T), (warp + 1) * per * kStep);
   const int32_t lane = threadIdx.x & 31;
   const int32_t last = static_cast<int32_t>(end) - 1;
-  const bool has_next = next.has != nullptr;
   int32_t doc = -1;
   for (int64_t step0 = begin; step0 < end; step0 += kStep) {
     const int32_t x_lo = static_cast<int32_t>(step0);
@@ -228,7 +238,7 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
       const int32_t c0 = cu[i];
       const int32_t c = m.div2(cu[i + 1] - c0);  // >= 1: document i holds row min(g, last)
       const int32_t off = min(g, last) - c0;
-      const int32_t k = off / c;                 // chunk 0 .. 2cp-1
+      const int32_t k = chunk_of(off, c);        // chunk 0 .. 2cp-1
       const bool front = k < m.cp;
       const int32_t u = (front ? k : 2 * m.cp - 1 - k) * S + m.div(c0) + (front ? 0 : c) + (off - k * c);
       const int32_t e = c0 + (cu_v[i + 1] - cu_v[i]);  // end of the document's valid tokens
@@ -248,7 +258,7 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
       for (int q = 0; q < kGroups; ++q) {
         if (!ok[q]) continue;
         uint8_t mk = k < room[q] ? 1 : 0;
-        if (k == room[q] && has_next && next.has[iq[q]] != 0) {  // the document's next token, one past its end
+        if (NEXT && k == room[q] && next.has[iq[q]] != 0) {  // the document's next token, one past its end
           v[q] = next.tok[iq[q]];
           mk = 1;
         }
@@ -274,11 +284,16 @@ thd_status_t launch_roll_labels_zigzag(const int32_t* tokens, const int32_t* cu_
   if (grid < 1) grid = 1;
   const CpMath m = make_cp_math(cp);
   const dim3 blocks(static_cast<unsigned>(grid));
+  const bool nx = has_next != nullptr;
   const cudaError_t e =
-      in_smem ? launch_smem(roll_labels_zigzag_kernel<true>, blocks, bytes, s, tokens, cu_v, cu, n, T, m, depth, fill,
-                            next, labels, lmask, valid, status)
-              : launch_smem(roll_labels_zigzag_kernel<false>, blocks, 0, s, tokens, cu_v, cu, n, T, m, depth, fill,
-                            next, labels, lmask, valid, status);
+      in_smem ? (nx ? launch_smem(roll_labels_zigzag_kernel<true, true>, blocks, bytes, s, tokens, cu_v, cu, n, T, m,
+                                  depth, fill, next, labels, lmask, valid, status)
+                    : launch_smem(roll_labels_zigzag_kernel<true, false>, blocks, bytes, s, tokens, cu_v, cu, n, T, m,
+                                  depth, fill, next, labels, lmask, valid, status))
+              : (nx ? launch_smem(roll_labels_zigzag_kernel<false, true>, blocks, 0, s, tokens, cu_v, cu, n, T, m,
+                                  depth, fill, next, labels, lmask, valid, status)
+                    : launch_smem(roll_labels_zigzag_kernel<false, false>, blocks, 0, s, tokens, cu_v, cu, n, T, m,
+                                  depth, fill, next, labels, lmask, valid, status));
   if (e != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
