@@ -28,10 +28,12 @@ class CpExchange:
     Calling it with this rank's shard of the source layout ([S, ...] rows)
     returns its shard of the target layout.  ``pack`` and ``scatter`` map
     (tensor, out or None) -> tensor; from_route binds libthd's per-rank
-    kernels to them."""
+    kernels to them.  ``all_to_all`` is the collective, called as
+    all_to_all(out, inp, output_split_sizes=..., input_split_sizes=...,
+    group=...); by default torch.distributed.all_to_all_single."""
 
     def __init__(self, cp_rank: int, input_split_sizes, output_split_sizes, send_identity: bool,
-                 recv_identity: bool, pack, scatter, group=None):
+                 recv_identity: bool, pack, scatter, group=None, all_to_all=None):
         self.cp_rank = int(cp_rank)
         self.input_split_sizes = [int(v) for v in input_split_sizes]
         self.output_split_sizes = [int(v) for v in output_split_sizes]
@@ -45,9 +47,10 @@ class CpExchange:
         self.recv_identity = bool(recv_identity)
         self._pack, self._scatter = pack, scatter
         self.group = group
+        self._all_to_all = all_to_all if all_to_all is not None else dist.all_to_all_single
 
     @classmethod
-    def from_route(cls, route, cp_rank: int, group=None, stream=None) -> "CpExchange":
+    def from_route(cls, route, cp_rank: int, group=None, stream=None, all_to_all=None) -> "CpExchange":
         """Read this rank's split sizes and identity flags from a device
         route (one synchronisation of ``stream``) and bind libthd's per-rank
         pack and scatter.  Raises ThdError when the route's build recorded an
@@ -90,15 +93,15 @@ class CpExchange:
         def scatter(recv, out):
             return api.scatter_rank(recv, route, r, out=out, stream=s)
 
-        return cls(r, ins, outs, send_id, recv_id, pack, scatter, group)
+        return cls(r, ins, outs, send_id, recv_id, pack, scatter, group, all_to_all)
 
     def __call__(self, shard: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
         if shard.dim() < 1 or shard.shape[0] != self.rows:
             raise ValueError(f"the shard must have {self.rows} rows, got shape {tuple(shard.shape)}")
         send = shard.contiguous() if self.send_identity else self._pack(shard, None)
         recv = torch.empty_like(send)
-        dist.all_to_all_single(recv, send, output_split_sizes=self.output_split_sizes,
-                               input_split_sizes=self.input_split_sizes, group=self.group)
+        self._all_to_all(recv, send, output_split_sizes=self.output_split_sizes,
+                         input_split_sizes=self.input_split_sizes, group=self.group)
         if self.recv_identity:
             if out is None:
                 return recv
