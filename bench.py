@@ -67,6 +67,8 @@ def parse_args():
     p.add_argument("--cp-exchange", action="store_true",
                    help="one CP rank per GPU (--gpus = the workload's cp): the conversion between GPUs, "
                         "per-rank pack -> NCCL all-to-all -> per-rank scatter, instead of independent replicas")
+    p.add_argument("--only-prep-at-scale", action="store_true",
+                   help="run only the data-preparation kernels at 16.8 M tokens and print their timings")
     p.add_argument("--no-other-configs", action="store_true",
                    help="skip the swap / route timings of the other full-size workloads")
     return p.parse_args()
@@ -1093,6 +1095,17 @@ def main():
             return
         if not torch.cuda.is_available():
             raise SystemExit("bench.py: the thd arm needs a CUDA GPU")
+        if args.only_prep_at_scale:
+            import context_packed_sequence_gb300 as thd
+            from context_packed_sequence_gb300 import _lib as L
+            device = torch.device("cuda", local)
+            torch.cuda.set_device(device)
+            clocks = ClockSampler(smi_gpu_id(device)).start()
+            prep = run_prep_at_scale(thd, L.load(), device, torch.cuda.current_stream(device), thd.new_status(device))
+            res = {"data_prep_at_scale": prep, "clocks": clocks.stop()}
+            if rank == 0:
+                print(json.dumps(res), flush=True)
+            return
         if args.cp_exchange:
             res = run_cp_exchange(args, rank, world, local)
             if rank == 0:
