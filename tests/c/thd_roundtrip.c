@@ -3,7 +3,11 @@
  * tiny workload (cp=2, documents [8, 12, 4]), swaps zigzag -> contiguous and
  * back, and checks against zigzag positions derived by hand from the
  * partition rule ("Packed Sequence 与上下文并行", section 2.4): rank 0 holds
- * chunks 0 and 3 of every document, rank 1 chunks 1 and 2.
+ * chunks 0 and 3 of every document, rank 1 chunks 1 and 2.  Then the same
+ * conversion through both routes bound into one shared buffer, as a batched
+ * swap of two [T][ROW] blocks, and as every rank's pack -> exchange ->
+ * scatter on its own shard (the exchange done here by copies, with the split
+ * sizes and offsets read back from the route).
  * Exit status 0 and "ok" on success.
  */
 #include <stdint.h>
@@ -94,6 +98,55 @@ int main(void) {
   }
   /* a bad direction is refused on the host */
   if (thd_route_build(cu, 3, T, CP, (thd_dir_t)7, &fwd, status, 0) != THD_ERR_BAD_DIRECTION) return 8;
+
+  /* both routes in one shared buffer; two [T][ROW] blocks in one batched swap */
+  {
+    thd_route_t pf, pb;
+    unsigned char *blob = NULL, *x2 = NULL, *y2 = NULL, *send = NULL, *recv = NULL, *w = NULL;
+    unsigned char host_y2[2 * T * ROW], host_w[T * ROW];
+    int32_t in_split[CP * CP], send_off[CP * (CP + 1)], recv_off[CP * (CP + 1)];
+    size_t pbytes = thd_route_pair_bytes(T, CP);
+    CHECK_CUDA(cudaMalloc((void **)&blob, pbytes));
+    CHECK_CUDA(cudaMalloc((void **)&x2, 2 * sizeof host_x));
+    CHECK_CUDA(cudaMalloc((void **)&y2, 2 * sizeof host_x));
+    CHECK_CUDA(cudaMalloc((void **)&send, sizeof host_x));
+    CHECK_CUDA(cudaMalloc((void **)&recv, sizeof host_x));
+    CHECK_CUDA(cudaMalloc((void **)&w, sizeof host_x));
+    CHECK_THD(thd_route_bind_pair(&pf, &pb, blob, pbytes, T, CP));
+    if (pf.recv_rows != pb.send_rows || pf.send_rows != pb.recv_rows) return 9;
+    CHECK_THD(thd_route_build_pair(cu, 3, T, CP, &pf, &pb, status, 0));
+    CHECK_CUDA(cudaMemcpy(x2, x, sizeof host_x, cudaMemcpyDeviceToDevice));
+    CHECK_CUDA(cudaMemcpy(x2 + sizeof host_x, x, sizeof host_x, cudaMemcpyDeviceToDevice));
+    CHECK_THD(thd_swap_batched(x2, y2, 2, ROW, &pf, status, 0));
+    /* every rank packs its own shard, the blocks go to their ranks, every rank scatters */
+    for (int r = 0; r < CP; ++r) CHECK_THD(thd_pack_rank(x + r * S * ROW, send + r * S * ROW, r, ROW, &pf, status, 0));
+    CHECK_CUDA(cudaMemcpy(in_split, pf.input_split_sizes, sizeof in_split, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(send_off, pf.send_offsets, sizeof send_off, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(recv_off, pf.recv_offsets, sizeof recv_off, cudaMemcpyDeviceToHost));
+    for (int s = 0; s < CP; ++s)
+      for (int d = 0; d < CP; ++d)
+        CHECK_CUDA(cudaMemcpy(recv + (d * S + recv_off[d * (CP + 1) + s]) * ROW,
+                              send + (s * S + send_off[s * (CP + 1) + d]) * ROW,
+                              (size_t)in_split[s * CP + d] * ROW, cudaMemcpyDeviceToDevice));
+    for (int r = 0; r < CP; ++r)
+      CHECK_THD(thd_scatter_rank(recv + r * S * ROW, w + r * S * ROW, r, ROW, &pf, status, 0));
+    CHECK_THD(thd_status_read(status, &code, 0));
+    if (code != THD_OK) {
+      fprintf(stderr, "device status %d\n", code);
+      return 10;
+    }
+    CHECK_CUDA(cudaMemcpy(host_y2, y2, sizeof host_y2, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(host_w, w, sizeof host_w, cudaMemcpyDeviceToHost));
+    if (memcmp(host_y2, host_y, sizeof host_y) != 0 || memcmp(host_y2 + sizeof host_y, host_y, sizeof host_y) != 0) {
+      fprintf(stderr, "batched swap differs from the swap\n");
+      return 11;
+    }
+    if (memcmp(host_w, host_y, sizeof host_y) != 0) {
+      fprintf(stderr, "per-rank pack / exchange / scatter differs from the swap\n");
+      return 12;
+    }
+    cudaFree(blob); cudaFree(x2); cudaFree(y2); cudaFree(send); cudaFree(recv); cudaFree(w);
+  }
 
   cudaFree(cu); cudaFree(status); cudaFree(idx); cudaFree(x); cudaFree(y); cudaFree(z);
   cudaFree(blob_f); cudaFree(blob_b);

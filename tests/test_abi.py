@@ -152,3 +152,52 @@ def test_host_checks_return_before_any_launch(lib):
     # two int64 per row, seven per 2048-token chunk (8 rows x 2 chunks), two totals
     assert lib.thd_pack_docs_workspace_bytes(8, 4096) == 8 * (2 * 8 + 7 * 16 + 2)
     assert lib.thd_status_clear(None, None) == L.ERR_INVALID_ARG
+
+
+def test_route_pair_bind_host_only(lib):
+    """thd_route_bind_pair: one buffer, the shared arrays aliased between the
+    two routes, every array 256-byte aligned and inside the buffer."""
+    T, cp = 48, 4
+    nbytes = lib.thd_route_pair_bytes(T, cp)
+    assert nbytes > 0 and nbytes < 2 * lib.thd_route_bytes(T, cp)
+    assert lib.thd_route_pair_bytes(50, 4) == 0
+    zc, cz = L.ThdRoute(), L.ThdRoute()
+    fake = 1 << 20
+    assert lib.thd_route_bind_pair(ctypes.byref(zc), ctypes.byref(cz), fake, nbytes, T, cp) == L.OK
+    assert (zc.dir, cz.dir) == (0, 1) and zc.total_rows == cz.total_rows == T
+    assert zc.recv_rows == cz.send_rows and zc.send_rows == cz.recv_rows
+    assert zc.src_of_dst != cz.src_of_dst
+    ptrs = []
+    for r in (zc, cz):
+        ptrs += [r.send_rows, r.recv_rows, r.src_of_dst, r.input_split_sizes, r.output_split_sizes,
+                 r.send_offsets, r.recv_offsets, r.send_identity, r.recv_identity]
+    assert all(p % 256 == 0 and fake <= p < fake + nbytes for p in ptrs)
+    assert len(set(ptrs)) == len(ptrs) - 2          # exactly the two shared arrays repeat
+    assert lib.thd_route_bind_pair(ctypes.byref(zc), ctypes.byref(cz), fake, nbytes - 1, T, cp) == L.ERR_INVALID_ARG
+    assert lib.thd_route_bind_pair(ctypes.byref(zc), ctypes.byref(cz), fake + 8, nbytes, T, cp) == L.ERR_INVALID_ARG
+    assert lib.thd_route_bind_pair(ctypes.byref(zc), ctypes.byref(zc), fake, nbytes, T, cp) == L.ERR_INVALID_ARG
+    assert lib.thd_route_bind_pair(None, ctypes.byref(cz), fake, nbytes, T, cp) == L.ERR_INVALID_ARG
+
+
+def test_batched_and_per_rank_host_checks(lib):
+    """thd_swap_batched, thd_pack_rank and thd_scatter_rank refuse bad
+    arguments before any launch."""
+    T, cp = 24, 2
+    r = L.ThdRoute()
+    fake = 1 << 20
+    lib.thd_route_bind(ctypes.byref(r), fake, lib.thd_route_bytes(T, cp), T, cp, 0)
+    big = 1 << 32
+    assert lib.thd_swap_batched(big, big + 3 * T * 16 - 16, 3, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
+    assert lib.thd_swap_batched(big, big + 4096, -1, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
+    assert lib.thd_swap_batched(big, big + 4096, (1 << 31) // T + 1, 4, ctypes.byref(r), None,
+                                None) == L.ERR_INVALID_ARG                      # outer * T above 2^31 - 1
+    assert lib.thd_swap_batched(big, big + 4096, 2, 0, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
+    assert lib.thd_swap_batched(big, big + 4096, 2, 16, None, None, None) == L.ERR_INVALID_ARG
+    assert lib.thd_swap_batched(None, None, 0, 16, ctypes.byref(r), None, None) == L.OK   # nothing to move
+    S = T // cp
+    for fn in (lib.thd_pack_rank, lib.thd_scatter_rank):
+        assert fn(big, big + S * 16, cp, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG   # rank >= cp
+        assert fn(big, big + S * 16, -1, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
+        assert fn(big, big + 8, 0, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG         # overlap
+        assert fn(big, None, 0, 16, ctypes.byref(r), None, None) == L.ERR_INVALID_ARG
+        assert fn(big, big + 4096, 0, 16, None, None, None) == L.ERR_INVALID_ARG
