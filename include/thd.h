@@ -351,11 +351,20 @@ thd_status_t thd_roll_labels_zigzag(const int32_t *tokens, const int32_t *cu_seq
  *                     does not end with EOD; else 0 (for thd_roll_labels)
  *  counts             device int64[2]: {num_docs, T} on completion
  *  workspace          device, >= thd_pack_docs_workspace_bytes(B, S) bytes,
- *                     8-byte aligned; scratch between the kernels (one int64
- *                     per row and four per 2048-token chunk).
+ *                     8-byte aligned; scratch of the call (its contents on
+ *                     entry do not matter; calls that may overlap on the GPU
+ *                     need separate workspaces).
  *  d_status           device int32[1], required; THD_ERR_CAPACITY when
- *                     num_docs+1 > docs_capacity or T > tokens_capacity (then
- *                     nothing but counts is written).
+ *                     num_docs+1 > docs_capacity or T > tokens_capacity: then
+ *                     counts holds the sizes needed, nothing is written past
+ *                     either capacity and the other outputs are unspecified.
+ *                     THD_ERR_TIMEOUT when a bounded wait of the single pass
+ *                     (below) ran out (outputs unspecified).
+ * From 2^22 raw tokens, with 16-byte aligned raw rows of a multiple of 4
+ * tokens, a 16-byte aligned tokens_out and align <= 65536, the call is one
+ * persistent kernel that reads every raw token once (6,144-token chunks
+ * taken in order; one block turns the chunks' published summaries into each
+ * chunk's offsets); otherwise three kernels (statistics, scan, emit).
  * The number of documents and T are only known on the device; a caller that
  * needs them on the host reads `counts` (one synchronisation, at data-prep
  * time).  T <= B*S*align and num_docs <= B*S always hold.

@@ -64,7 +64,8 @@ def test_debug_header_links_against_the_checked_build(tmp_path):
                    "int main(void) {\n"
                    "  thd_status_t (*a)(cudaStream_t) = thd_debug_stall_next_bulk_copy;\n"
                    "  thd_status_t (*b)(cudaStream_t) = thd_debug_stall_next_ulysses_tile;\n"
-                   "  return (a != 0 && b != 0) ? 0 : 1;\n"
+                   "  thd_status_t (*c)(cudaStream_t) = thd_debug_stall_next_pack;\n"
+                   "  return (a != 0 && b != 0 && c != 0) ? 0 : 1;\n"
                    "}\n")
     exe = str(tmp_path / "debug")
     cmd = [cc, "-std=c11", "-Wall", "-Werror", "-O2", str(src), "-o", exe,

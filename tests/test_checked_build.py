@@ -2,8 +2,8 @@
 THD_CHECKED=1 is set) range-checks every row index its kernels compute in
 closed form and reports a miss as THD_ERR_INDEX_RANGE instead of touching
 memory.  On the CPU: it builds and exports the same C ABI.  On the GPU: the
-parity (including the per-rank copies, the batched swap and packing without
-allocation), error and maximum-size suites pass against it unchanged, so no
+parity (including the per-rank copies, the batched swap, packing without
+allocation and the single-pass packing), error and maximum-size suites pass against it unchanged, so no
 computed index of any of those cases leaves its range."""
 
 import ctypes
@@ -47,7 +47,7 @@ def test_checked_build_exports_the_abi(checked_lib):
 def test_gpu_suites_pass_on_the_checked_build(checked_lib):
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
            "tests/test_parity.py", "tests/test_rank_and_batched.py", "tests/test_errors.py", "tests/test_max_size.py",
-           "tests/test_zz_no_alloc.py"]
+           "tests/test_zz_no_alloc.py", "tests/test_pack_onepass.py"]
     r = subprocess.run(cmd, cwd=ROOT, env=_checked_env(), capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
