@@ -43,8 +43,12 @@ constexpr int kPackThreads = 1024;
 constexpr int kItems = 8;  // consecutive tokens per thread per tile
 constexpr int64_t kTile = static_cast<int64_t>(kPackThreads) * kItems;
 
+// (-L) mod align for L >= 0: a mask when align is a power of two (the usual
+// 2 * cp), a 32-bit remainder for lengths below 2^32
 __device__ __forceinline__ int64_t pad_of(int64_t L, int32_t align) {
-  int64_t r = L % align;
+  if ((align & (align - 1)) == 0) return (-L) & (align - 1);
+  const int64_t r = (L >> 32) == 0 ? static_cast<int64_t>(static_cast<uint32_t>(L) % static_cast<uint32_t>(align))
+                                   : L % align;
   return r == 0 ? 0 : align - r;
 }
 
@@ -1080,7 +1084,7 @@ pack_onepass_kernel(const int32_t* raw, ChunkGeom g, OnePassArgs a) {
   // per buffer: its chunk (>= nc: none), that chunk's row's valid end, the
   // chunk's scan total, its first and last end (relative) and whether its
   // tokens failed to land
-  __shared__ int64_t sh_z[kBufs], sh_ve[kBufs], sh_total[kBufs];
+  __shared__ int64_t sh_z[kBufs], sh_ve[kBufs], sh_total[kBufs], sh_row[kBufs], sh_lo[kBufs];
   __shared__ int32_t sh_first[kBufs], sh_last[kBufs], sh_bad[kBufs];
   __shared__ Carry sh_carry;
   __shared__ int32_t sh_role;
@@ -1111,15 +1115,18 @@ pack_onepass_kernel(const int32_t* raw, ChunkGeom g, OnePassArgs a) {
       const int64_t row = z / g.per_row, lo = (z - row * g.per_row) * g.chunk;
       const uint32_t bytes = static_cast<uint32_t>(min(g.chunk, g.S - lo) * sizeof(int32_t));
       sh_ve[b] = a.ve ? a.ve[row] : g.S;
+      sh_row[b] = row;
+      sh_lo[b] = lo;
       mbar_arrive_expect_tx(&bars[b], bytes);
       bulk_load(tokens_of(b), raw + row * g.S + lo, bytes, &bars[b]);
     }
   };
-  // the valid tokens [0, n_valid) of chunk z relative to its first token, and
-  // the row's last valid token (-1: not in this chunk)
-  auto chunk_span = [&](int64_t z, int64_t ve, int64_t* row, int64_t* lo, int32_t* n_valid, int32_t* last_valid) {
-    *row = z / g.per_row;
-    *lo = (z - *row * g.per_row) * g.chunk;
+  // the chunk in buffer b: its row and first token, its valid tokens
+  // [0, n_valid) relative to that token, and the row's last valid token (-1:
+  // not in this chunk)
+  auto chunk_span = [&](int b, int64_t ve, int64_t* row, int64_t* lo, int32_t* n_valid, int32_t* last_valid) {
+    *row = sh_row[b];
+    *lo = sh_lo[b];
     *n_valid = static_cast<int32_t>(max(int64_t(0), min(g.chunk, ve - *lo)));
     *last_valid = ve - *lo - 1 < g.chunk ? static_cast<int32_t>(ve - *lo - 1) : -1;
   };
@@ -1130,7 +1137,7 @@ pack_onepass_kernel(const int32_t* raw, ChunkGeom g, OnePassArgs a) {
     const int64_t z = sh_z[b];
     int64_t row, lo;
     int32_t n_valid, last_valid;
-    chunk_span(z, sh_ve[b], &row, &lo, &n_valid, &last_valid);
+    chunk_span(b, sh_ve[b], &row, &lo, &n_valid, &last_valid);
     const bool landed = mbar_wait(&bars[b], (phase_bits >> b) & 1u);
     phase_bits ^= 1u << b;
     RelEnds te;
@@ -1225,7 +1232,7 @@ pack_onepass_kernel(const int32_t* raw, ChunkGeom g, OnePassArgs a) {
     int64_t row, lo;
     int32_t n_valid, last_valid;
     const int64_t ve = sh_ve[be];
-    chunk_span(zE, ve, &row, &lo, &n_valid, &last_valid);
+    chunk_span(be, ve, &row, &lo, &n_valid, &last_valid);
     const int32_t* const tok = tokens_of(be);
     const uint32_t* const ends = ends_of(be);
     const uint32_t my_ends = ends[threadIdx.x];
