@@ -50,6 +50,8 @@ struct NextTokens {
 // 16-byte store and its four masks with one 4-byte store (VEC: T a multiple
 // of 4, labels 16-byte and masks 4-byte aligned), else one position at a time.
 constexpr int kPerLane = 4;
+// tokens kept per lane for four consecutive rows: four rows, depths up to 7
+constexpr int kZzWindow = kPerLane + 7;
 
 template <bool SMEM_CU, bool VEC>
 __global__ void __launch_bounds__(kLabelThreads)
@@ -125,6 +127,33 @@ roll_labels_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_v_g, co
       *reinterpret_cast<uint32_t*>(valid + p0) = vbits;
     } else {
       for (int t = 0; t < kPerLane && p0 + t <= last; ++t) valid[p0 + t] = static_cast<uint8_t>(vbits >> (8 * t));
+    }
+    // four positions of one document, depths within the window: one window
+    // of tokens serves every depth (position p0 + t at depth k reads token
+    // p0 + 1 + t + k while t + k < R)
+    if (VEC && full && di[0] == di[kPerLane - 1] && depth <= kZzWindow - kPerLane) {
+      const int32_t R = ei[0] - p0 - 1;
+      int32_t w[kZzWindow];
+#pragma unroll
+      for (int x = 0; x < kZzWindow; ++x) w[x] = x <= depth + kPerLane - 1 && x < R ? __ldg(tokens + p0 + 1 + x) : fill;
+      const bool has = next.has != nullptr && next.has[di[0]] != 0;
+      const int32_t nt = has ? next.tok[di[0]] : fill;
+#pragma unroll
+      for (int k = 0; k <= kZzWindow - kPerLane; ++k) {
+        if (k > depth) break;
+        int32_t v[kPerLane];
+        uint32_t mbits = 0;
+#pragma unroll
+        for (int t = 0; t < kPerLane; ++t) {
+          const bool in = t + k < R, at_end = t + k == R && has;
+          v[t] = in ? w[t + k] : (at_end ? nt : fill);
+          mbits |= (in || at_end ? 1u : 0u) << (8 * t);
+        }
+        const int64_t o = static_cast<int64_t>(k) * T + p0;
+        *reinterpret_cast<int4*>(labels + o) = make_int4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<uint32_t*>(lmask + o) = mbits;
+      }
+      continue;
     }
     for (int32_t k = 0; k <= depth; ++k) {
       int32_t v[kPerLane];
@@ -311,7 +340,6 @@ roll_labels_zigzag_kernel(const int32_t* __restrict__ tokens, const int32_t* cu_
 // consecutive rows whenever they stay in one rank, one document and one
 // chunk (all but a few lanes in a hundred on documents of a few hundred
 // slots); the others take each position on its own.
-constexpr int kZzWindow = 4 + 7;  // rows' tokens kept per lane: four rows, depths up to 7
 
 template <bool SMEM_CU, bool NEXT>
 __global__ void __launch_bounds__(kLabelThreads)
