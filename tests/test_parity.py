@@ -499,6 +499,35 @@ def test_roll_labels_zigzag_parity(cp, depth):
         assert got[2].cpu().tolist() == want[2]
 
 
+@pytest.mark.parametrize("cp,depth", [(2, 7), (3, 7), (8, 9), (4, 12)])
+def test_labels_deep_mtp_both_layouts(cp, depth):
+    """MTP depths at and past the seven that the label kernels' token window
+    holds (then they read each depth's tokens on their own), with extra
+    tokens, in both layouts, against the oracle."""
+    rng = np.random.default_rng(900 + 10 * cp + depth)
+    for trial in range(6):
+        n = int(rng.integers(1, 60))
+        lp = [2 * cp * int(rng.integers(0, 14)) for _ in range(n)]
+        lv = [min(L, int(rng.integers(0, L + 3))) if L else 0 for L in lp]
+        cu_v, cu = _bounds(lv), _bounds(lp)
+        T = cu[-1]
+        tokens = [int(t) for t in rng.integers(0, 151936, size=T)]
+        nxt = [int(rng.integers(200000, 300000)) if (L and rng.random() < 0.4) else None for L in lv]
+        nt = torch.tensor([v or 0 for v in nxt], dtype=torch.int32, device="cuda")
+        hn = torch.tensor([int(v is not None) for v in nxt], dtype=torch.uint8, device="cuda")
+        tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+        st = thd.new_status()
+        got = thd.roll_labels(tok, _cu_tensor(cu_v), _cu_tensor(cu), depth, -9, status=st, next_token=nt,
+                              has_next=hn)
+        got_z = thd.roll_labels_zigzag(tok, _cu_tensor(cu_v), _cu_tensor(cu), cp, depth, -9, status=st,
+                                       next_token=nt, has_next=hn)
+        thd.check_status(st)
+        assert [g.cpu().tolist() for g in got] == [list(w) for w in oracle.roll_labels(tokens, cu_v, cu, depth,
+                                                                                      fill=-9, doc_next=nxt)]
+        assert [g.cpu().tolist() for g in got_z] == [list(w) for w in oracle.roll_labels_zigzag(
+            tokens, cu_v, cu, cp, depth, fill=-9, doc_next=nxt)]
+
+
 @pytest.mark.parametrize("cp,n", [(1, 13000), (4, 13000), (4, 24000)])
 def test_labels_and_partition_beyond_shared_memory(cp, n):
     """Many documents (empty ones included): with 13,000 the label kernels
