@@ -1061,20 +1061,21 @@ __device__ __forceinline__ void rec_peek(const int64_t* rec, uint64_t (&w)[4]) {
 }
 
 // The blocks that pack (every block but the scanner).  A block works on a
-// ring of kBufs chunks.  In iteration i it
-//   (a) sets out to take chunk i + 1 (the counter's answer is used after (b),
-//       when thread 0 starts that chunk's bulk load into its buffer, free
-//       since its chunk was written);
-//   (b) summarises chunk i (its tokens were requested one iteration ago) and
-//       publishes the summary; every thread keeps its ends, the last end
-//       before it and the padded tokens before it in the buffer;
-//   (c) writes chunk i - kLag, whose carries the scanner has had kLag
+// ring of kBufs chunks; call the chunks it takes, in order, its chunks 0, 1,
+// 2, ...  In iteration i it
+//   (a) sets out to take its chunk i + 1 (the counter's answer is used after
+//       (b), when thread 0 starts that chunk's bulk load into its buffer,
+//       free since the chunk that held it was written);
+//   (b) summarises its chunk i (whose tokens were requested one iteration
+//       ago) and publishes the summary; every thread keeps its ends, the
+//       last end before it and the padded tokens before it in the buffer;
+//   (c) writes its chunk i - kLag, whose carries the scanner has had kLag
 //       iterations to publish: every document end writes its boundaries,
 //       padding and the shift of the next document's tokens, then the block
 //       copies the tokens with consecutive threads on consecutive tokens.
 // A chunk held between its summary and its writing delays no one (its
-// summary is out); the one chunk held without a summary, i + 1, is only
-// ever waited for by chunks after it.
+// summary is out); the one chunk held without a summary, i + 1, has a
+// larger number than every chunk the block waits for.
 __global__ void __launch_bounds__(kOneThreads, kOneBlocksPerSm)
 pack_onepass_kernel(const int32_t* raw, ChunkGeom g, OnePassArgs a) {
   extern __shared__ __align__(16) int32_t one_smem[];
@@ -1082,8 +1083,8 @@ pack_onepass_kernel(const int32_t* raw, ChunkGeom g, OnePassArgs a) {
   __shared__ int64_t scan_b[64];
   __shared__ uint64_t bars[kBufs];
   // per buffer: its chunk (>= nc: none), that chunk's row's valid end, the
-  // chunk's scan total, its first and last end (relative) and whether its
-  // tokens failed to land
+  // chunk's scan total, row and first token, its first and last end
+  // (relative to that token) and whether its tokens failed to land
   __shared__ int64_t sh_z[kBufs], sh_ve[kBufs], sh_total[kBufs], sh_row[kBufs], sh_lo[kBufs];
   __shared__ int32_t sh_first[kBufs], sh_last[kBufs], sh_bad[kBufs];
   __shared__ Carry sh_carry;
