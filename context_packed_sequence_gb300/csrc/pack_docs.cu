@@ -24,7 +24,7 @@
 //         stores every chunk's carries;
 //      3. emit: every chunk writes its tokens, padding and boundaries.
 //    Scratch: two int64 per row, seven per chunk and two totals.
-//  * single pass (thd_pack_docs from 2^22 raw tokens, aligned rows and
+//  * single pass (thd_pack_docs from 2^19 raw tokens, aligned rows and
 //    output): one persistent kernel reads every token once; blocks take
 //    6,144-token chunks in order, publish each chunk's summary, and write it
 //    once a scanner block has turned the summaries before it into the
@@ -293,6 +293,10 @@ pack_emit_kernel(const int32_t* raw, int32_t B, int64_t S, int32_t eod, int32_t 
 constexpr int kChunkThreads = 512;
 constexpr int64_t kSmallChunk = static_cast<int64_t>(kChunkThreads) * 4;
 constexpr int64_t kBigChunkFrom = int64_t(1) << 22;  // tokens per batch
+// The single pass from this many raw tokens per batch: measured on GB300
+// against the chunked kernels, 1.3x faster at 2^20 and 1.5x at 2^21, 1.3x
+// slower at 2^18 (where both are bound by launch latency)
+constexpr int64_t kOnePassFrom = int64_t(1) << 19;
 
 // documents and padded tokens of a thread or chunk in one word: the count
 // fits 14 bits (at most 8,192 ends per chunk), the padded tokens the rest
@@ -681,7 +685,7 @@ pack_chunk_emit_kernel(const int32_t* raw, ChunkGeom g, int32_t eod, const int64
 // single pass (large batches of aligned rows)
 // ---------------------------------------------------------------------------
 //
-// From 2^22 raw tokens per batch, with 16-byte aligned rows of a multiple of
+// From 2^19 raw tokens per batch, with 16-byte aligned rows of a multiple of
 // 4 tokens, a 16-byte aligned output and an alignment of at most 65,536, one
 // persistent kernel packs every 6,144-token chunk reading its tokens once
 // (the three kernels above read them twice and wait for each other between
@@ -1482,7 +1486,8 @@ thd_status_t launch_pack_docs(const int32_t* raw, int32_t B, int64_t S, int32_t 
   while ((int64_t(1) << shift) < S) ++shift;
   const bool keys_fit = shift < 62 && (static_cast<int64_t>(B) >> (61 - shift)) == 0;
   // (and keeps a chunk's padded tokens before a thread in 31 bits)
-  if (big && vec && keys_fit && align <= 65536 && reinterpret_cast<uintptr_t>(tokens) % 16 == 0)
+  if (static_cast<int64_t>(B) * S >= kOnePassFrom && vec && keys_fit && align <= 65536 &&
+      reinterpret_cast<uintptr_t>(tokens) % 16 == 0)
     return launch_pack_onepass(raw, B, S, eod, trim, raw_pad, align, pad_id, row_next, tokens, tok_cap, cu_v, cu,
                                next_tok, has_next, docs_cap, counts, ws, status, s);
   ChunkGeom g;

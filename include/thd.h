@@ -360,7 +360,7 @@ thd_status_t thd_roll_labels_zigzag(const int32_t *tokens, const int32_t *cu_seq
  *                     either capacity and the other outputs are unspecified.
  *                     THD_ERR_TIMEOUT when a bounded wait of the single pass
  *                     (below) ran out (outputs unspecified).
- * From 2^22 raw tokens, with 16-byte aligned raw rows of a multiple of 4
+ * From 2^19 raw tokens, with 16-byte aligned raw rows of a multiple of 4
  * tokens, a 16-byte aligned tokens_out and align <= 65536, the call is one
  * persistent kernel that reads every raw token once (6,144-token chunks
  * taken in order; one block turns the chunks' published summaries into each

@@ -35,7 +35,7 @@ thd_status_t thd_debug_stall_next_bulk_copy(cudaStream_t stream);
 thd_status_t thd_debug_stall_next_ulysses_tile(cudaStream_t stream);
 
 /*
- * One-shot, for thd_pack_docs on the single-pass path (from 2^22 raw tokens,
+ * One-shot, for thd_pack_docs on the single-pass path (from 2^19 raw tokens,
  * 16-byte aligned rows of a multiple of 4 tokens and a 16-byte aligned
  * output): the block that takes chunk 0 of the next such call publishes no
  * summary, so the waits for it (the scanner's, and through it every block's

@@ -1,4 +1,4 @@
-"""The single-pass packing (thd_pack_docs from 2^22 raw tokens, 16-byte
+"""The single-pass packing (thd_pack_docs from 2^19 raw tokens, 16-byte
 aligned rows of a multiple of 4 tokens, 16-byte aligned output): one
 persistent kernel whose blocks take 8,192-token chunks in order and look back
 over the published summaries of the chunks before them.  Every output is
@@ -96,8 +96,23 @@ def test_rows_shorter_than_a_chunk():
     _check(raw, 7, 8, trim=True)
 
 
+def test_smallest_single_pass_batches():
+    """Just above and at the single pass's lower size (2^19 raw tokens): one
+    row, and many short rows with trimmed tails and extra tokens."""
+    rng = np.random.default_rng(310)
+    raw = rng.integers(1, 50, size=(1, 2**19)).astype(np.int32)
+    raw[rng.random(raw.shape) < 1 / 1000] = 7
+    _check(raw, 7, 16)
+    B, S = 128, 4096
+    raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+    raw[rng.random((B, S)) < 1 / 300] = 7
+    for b in range(0, B, 3):
+        raw[b, int(rng.integers(0, S + 1)):] = 0
+    _check(raw, 7, 8, trim=True, extra=rng.integers(100, 200, size=B).astype(np.int32))
+
+
 def test_unaligned_row_length_takes_the_chunked_kernels():
-    """S not a multiple of 4 at the same size: the three chunked kernels."""
+    """S not a multiple of 4 at a single-pass size: the three chunked kernels."""
     rng = np.random.default_rng(306)
     B, S = 2, 2**21 + 7
     raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
