@@ -1444,10 +1444,19 @@ thd_status_t launch_pack_onepass(const int32_t* raw, int32_t B, int64_t S, int32
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }
+  // the kernel's shared-memory size, set when the context does not have it
+  // yet (a query, so that a call made during stream capture only enqueues
+  // launches, and a reset context gets it again)
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, pack_onepass_kernel)) != cudaSuccess ||
+      (fa.maxDynamicSharedSizeBytes < static_cast<int>(kOneSmem) &&
+       (e = cudaFuncSetAttribute(pack_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kOneSmem))) != cudaSuccess)) {
+    record_cuda_error(e);
+    return THD_ERR_CUDA;
+  }
   if ((e = launch_pdl(pack_onepass_prepare_kernel, 1, 1024, 0, s, g.nc, a.ticket, recs,
-                      static_cast<const int64_t*>(a.ve), B, vbefore)) != cudaSuccess ||
-      (e = cudaFuncSetAttribute(pack_onepass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kOneSmem))) != cudaSuccess) {
+                      static_cast<const int64_t*>(a.ve), B, vbefore)) != cudaSuccess) {
     record_cuda_error(e);
     return THD_ERR_CUDA;
   }

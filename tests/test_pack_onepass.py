@@ -183,3 +183,83 @@ def test_look_back_wait_gives_up_on_a_flag_nobody_sets():
     tok, cu_v, cu = thd.pack_docs(x, 7, 8)
     assert np.array_equal(tok.cpu().numpy(), np.asarray(want[0], dtype=np.int32))
     assert cu.cpu().tolist() == want[2]
+
+
+def _raw_call(lib, x, B, S, outs, ws, st, stream):
+    tokens, cu_v, cu, counts = outs
+    return lib.thd_pack_docs(x.data_ptr(), B, S, 7, 0, 0, 8, 0, None, tokens.data_ptr(), tokens.numel(),
+                             cu_v.data_ptr(), cu.data_ptr(), None, None, cu.numel(), counts.data_ptr(),
+                             ws.data_ptr(), ws.numel(), st.data_ptr(), stream.cuda_stream)
+
+
+def _outputs(B, S, dev):
+    return (torch.empty(B * S * 8, dtype=torch.int32, device=dev), torch.empty(B * S + 1, dtype=torch.int32, device=dev),
+            torch.empty(B * S + 1, dtype=torch.int32, device=dev), torch.zeros(2, dtype=torch.int64, device=dev))
+
+
+def _assert_outputs(outs, want):
+    tokens, cu_v, cu, counts = outs
+    n, T = counts.tolist()
+    assert T == len(want[0]) and n == len(want[1]) - 1
+    assert np.array_equal(tokens[:T].cpu().numpy(), np.asarray(want[0], dtype=np.int32))
+    assert cu[:n + 1].cpu().tolist() == want[2] and cu_v[:n + 1].cpu().tolist() == want[1]
+
+
+def test_single_pass_in_a_cuda_graph():
+    """The single pass captured in a CUDA graph (the clearing kernel and the
+    persistent kernel) and replayed three times on changing input: every
+    replay clears the counters and records it uses."""
+    rng = np.random.default_rng(311)
+    B, S = 4, 2**18
+    lib = L.load()
+    dev = torch.device("cuda")
+    x = torch.empty((B, S), dtype=torch.int32, device=dev)
+    outs = _outputs(B, S, dev)
+    ws = torch.empty(lib.thd_pack_docs_workspace_bytes(B, S), dtype=torch.uint8, device=dev)
+    st = thd.new_status(dev)
+    side = torch.cuda.Stream()
+    x.copy_(torch.from_numpy(rng.integers(1, 50, size=(B, S)).astype(np.int32)))
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # one eager call first (loads the kernels into the context)
+        assert _raw_call(lib, x, B, S, outs, ws, st, side) == L.OK
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        assert _raw_call(lib, x, B, S, outs, ws, st, torch.cuda.current_stream()) == L.OK
+    for trial in range(3):
+        raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+        raw[rng.random(raw.shape) < (1 / 500, 1 / 5000, 1 / 50)[trial]] = 7
+        x.copy_(torch.from_numpy(raw))
+        g.replay()
+        torch.cuda.synchronize()
+        assert thd.status_read(st) == L.OK
+        _assert_outputs(outs, O.pack_docs(raw.tolist(), 7, 8))
+
+
+def test_two_streams_with_their_own_workspaces():
+    """Two single-pass calls that may overlap on the GPU (two streams, no
+    ordering between them), each with its own workspace and outputs."""
+    rng = np.random.default_rng(312)
+    B, S = 4, 2**18
+    lib = L.load()
+    dev = torch.device("cuda")
+    raws = []
+    for k in range(2):
+        raw = rng.integers(1, 50, size=(B, S)).astype(np.int32)
+        raw[rng.random(raw.shape) < (1 / 700, 1 / 3000)[k]] = 7
+        raws.append(raw)
+    xs = [torch.from_numpy(r).to(dev) for r in raws]
+    outs = [_outputs(B, S, dev) for _ in range(2)]
+    wss = [torch.empty(lib.thd_pack_docs_workspace_bytes(B, S), dtype=torch.uint8, device=dev) for _ in range(2)]
+    sts = [thd.new_status(dev) for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for k in range(2):
+            with torch.cuda.stream(streams[k]):
+                assert _raw_call(lib, xs[k], B, S, outs[k], wss[k], sts[k], streams[k]) == L.OK
+    torch.cuda.synchronize()
+    for k in range(2):
+        assert thd.status_read(sts[k]) == L.OK
+        _assert_outputs(outs[k], O.pack_docs(raws[k].tolist(), 7, 8))
